@@ -1,0 +1,180 @@
+"""Thin ctypes binding of libattn (include/attn.h), with the C ABI's names.
+
+Argument marshalling only: tensors become device pointers and sizes, the stream
+becomes a handle, a negative status becomes an exception. Every step of the
+computation runs in the library's CUDA kernels; there is no CPU path and no fallback.
+If the library has not been built the first call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_lib", "libattn.so")
+
+ATTN_BF16 = 0
+ATTN_F32 = 1
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_CUDA = -3
+ATTN_ERR_TIMEOUT = -4
+ATTN_ERR_WORKSPACE = -5
+ATTN_DEVERR_KVLEN = 0x1
+ATTN_DEVERR_TIMEOUT = 0x2
+
+EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_peek_device_error",
+            "attn_status_string", "attn_build_info", "attn_launch_count")
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libattn.so (once) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libattn.so is not built ({path}); run "
+                           "`python -m attention_sm_flash_gb300.build` first")
+    lib = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.attn_fwd.restype = i
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp]
+    lib.attn_bwd.restype = i
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp,
+                             i, vp, sz, vp]
+    lib.attn_bwd_workspace_size.restype = sz
+    lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
+    lib.attn_peek_device_error.restype = i
+    lib.attn_peek_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_status_string.argtypes = [i]
+    lib.attn_build_info.restype = ctypes.c_char_p
+    lib.attn_build_info.argtypes = []
+    lib.attn_launch_count.restype = ctypes.c_uint64
+    lib.attn_launch_count.argtypes = []
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().attn_status_string(int(status)).decode()
+
+
+def build_info() -> str:
+    return load().attn_build_info().decode()
+
+
+def attn_launch_count() -> int:
+    """Kernel launches the library has issued in this process."""
+    return int(load().attn_launch_count())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float32:
+        return ATTN_F32
+    raise TypeError(f"unsupported element type {t.dtype}")
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is not None and not isinstance(t, int):
+            if not t.is_cuda:
+                raise ValueError("libattn takes device tensors only")
+            if not t.is_contiguous():
+                raise ValueError("libattn takes contiguous tensors only")
+
+
+def attn_fwd(q, k, v, o, lse, causal: bool = False, scale: float | None = None,
+             kv_lens=None, stream=None) -> None:
+    """O and LSE of attention. q [B,Sq,Hq,D]; k, v [B,Skv,Hkv,D]; o like q; lse [B,Hq,Sq]."""
+    _check_cuda(q, k, v, o, lse, kv_lens)
+    B, Sq, Hq, D = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    st = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv,
+                         D, float(scale), int(bool(causal)), _ptr(kv_lens), _dtype_code(q),
+                         _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd")
+
+
+def attn_bwd_workspace_size(B: int, Hq: int, Sq: int, D: int, dtype_code: int) -> int:
+    return int(load().attn_bwd_workspace_size(B, Hq, Sq, D, dtype_code))
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal: bool = False,
+             scale: float | None = None, kv_lens=None, workspace=None, stream=None) -> None:
+    """dQ, dK, dV of sum(O * dO). ``workspace``: a uint8 device tensor of at least
+    attn_bwd_workspace_size() bytes; allocated here (by torch) when None."""
+    _check_cuda(q, k, v, o, dout, lse, dq, dk, dv, kv_lens)
+    B, Sq, Hq, D = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    code = _dtype_code(q)
+    need = attn_bwd_workspace_size(B, Hq, Sq, D, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                         _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Skv, D, float(scale),
+                         int(bool(causal)), _ptr(kv_lens), code, _ptr(workspace),
+                         workspace.numel(), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+
+
+def attn_peek_device_error(stream=None) -> tuple[int, int]:
+    """(status, raw ATTN_DEVERR_* bits) of the device error word, which it clears."""
+    bits = ctypes.c_uint32(0)
+    st = load().attn_peek_device_error(ctypes.byref(bits), _stream(stream))
+    return int(st), int(bits.value)
+
+
+def forward(q, k, v, causal=False, scale=None, kv_lens=None, stream=None):
+    """Allocate O and LSE (torch) and run attn_fwd."""
+    B, Sq, Hq, D = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, o, lse, causal, scale, kv_lens, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, dout, lse, causal=False, scale=None, kv_lens=None, stream=None):
+    """Allocate dQ, dK, dV (torch) and run attn_bwd."""
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal, scale, kv_lens, None, stream)
+    return dq, dk, dv

@@ -1,0 +1,175 @@
+// The C ABI of libattn (declared in include/attn.h): host-side argument checks, the
+// device error word, and the choice of kernel family by element type.
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+// The device error word: kernels OR ATTN_DEVERR_* bits into it.
+__device__ unsigned int g_error_word = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_err_addr[kMaxDevices] = {};
+
+// The error word's device address on the current device (looked up once per device).
+cudaError_t error_word(unsigned int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_error_word);
+    if (e != cudaSuccess) return e;
+    g_err_addr[dev] = static_cast<unsigned int*>(ptr);
+  }
+  *out = g_err_addr[dev];
+  return cudaSuccess;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks shared by the forward and the backward. Returns ATTN_OK, or the error.
+attn_status_t check_common(int B, int Hq, int Hkv, int Sq, int Skv, int D, float scale,
+                           int causal, const int32_t* kv_lens, attn_dtype_t dtype) {
+  if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  if (kv_lens != nullptr && !aligned(kv_lens, 4)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  // grid limits of the launch shapes: heads and batches index grid dimensions
+  if (Hq > 65535 || B > 65535) return ATTN_ERR_UNSUPPORTED;
+  // every element offset must fit a signed 64-bit integer with room to spare
+  const double elems_q = (double)B * Sq * Hq * D, elems_k = (double)B * Skv * Hkv * D;
+  if (elems_q > 4.0e18 || elems_k > 4.0e18) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+attn_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+std::atomic<uint64_t> g_launches{0};
+
+}  // namespace
+
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o,
+                                  float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                                  float scale, int causal, const int32_t* kv_lens,
+                                  attn_dtype_t dtype, attn_stream_t stream) {
+  attn_status_t st = check_common(B, Hq, Hkv, Sq, Skv, D, scale, causal, kv_lens, dtype);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || Sq == 0) return ATTN_OK;  // an empty problem: nothing to compute
+  if (q == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (Skv > 0 && (k == nullptr || v == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4))
+    return ATTN_ERR_INVALID_ARG;
+  Problem p{};
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.D = D;
+  p.scale = scale; p.causal = causal; p.kv_lens = kv_lens; p.dtype = dtype;
+  cudaError_t e = error_word(&p.err);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return from_cuda(simt_fwd(p, s));
+}
+
+extern "C" size_t attn_bwd_workspace_size(int B, int Hq, int Sq, int D, attn_dtype_t dtype) {
+  (void)D;
+  (void)dtype;
+  if (B <= 0 || Hq <= 0 || Sq <= 0) return 0;
+  const size_t delta = (size_t)B * Hq * Sq * sizeof(float);
+  return (delta + 255) / 256 * 256;
+}
+
+extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                                  const void* dout, const float* lse, void* dq, void* dk,
+                                  void* dv, int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                                  float scale, int causal, const int32_t* kv_lens,
+                                  attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                                  attn_stream_t stream) {
+  attn_status_t st = check_common(B, Hq, Hkv, Sq, Skv, D, scale, causal, kv_lens, dtype);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || (Sq == 0 && Skv == 0)) return ATTN_OK;
+  if (Sq == 0) {
+    // no queries: every key gets zero gradient; dk, dv are still outputs
+    if (dk == nullptr || dv == nullptr) return ATTN_ERR_INVALID_ARG;
+    const size_t elem = dtype == ATTN_F32 ? 4 : 2;
+    const size_t bytes = (size_t)B * Skv * Hkv * D * elem;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(dk, 0, bytes, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, bytes, s);
+    return from_cuda(e);
+  }
+  if (q == nullptr || o == nullptr || dout == nullptr || lse == nullptr || dq == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (Skv > 0 && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_bwd_workspace_size(B, Hq, Sq, D, dtype);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+    return ATTN_ERR_WORKSPACE;
+  Problem p{};
+  p.q = q; p.k = k; p.v = v; p.o_in = o; p.dout = dout; p.lse = const_cast<float*>(lse);
+  p.dq = dq; p.dk = dk; p.dv = dv; p.delta = static_cast<float*>(workspace);
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.D = D;
+  p.scale = scale; p.causal = causal; p.kv_lens = kv_lens; p.dtype = dtype;
+  cudaError_t e = error_word(&p.err);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return from_cuda(simt_bwd(p, s));
+}
+
+extern "C" attn_status_t attn_peek_device_error(uint32_t* bits, attn_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word));
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  const unsigned int zero = 0;
+  e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  if (bits != nullptr) *bits = word;
+  if (word & ATTN_DEVERR_TIMEOUT) return ATTN_ERR_TIMEOUT;
+  if (word & ATTN_DEVERR_KVLEN) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+extern "C" const char* attn_status_string(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG: invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: unsupported configuration";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA runtime error";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: device barrier wait timed out";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: workspace missing or too small";
+  }
+  return "unknown attn status";
+}
+
+extern "C" uint64_t attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+extern "C" const char* attn_build_info(void) {
+  return "libattn sm_103a: simt-fp32 fwd/bwd";
+}

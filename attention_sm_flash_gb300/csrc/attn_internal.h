@@ -1,0 +1,51 @@
+// Internal interface between the C ABI (attn_api.cu) and the kernel families.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/attn.h"
+
+namespace attn {
+
+// One validated attention problem. Every pointer is a device pointer.
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;            // forward output
+  float* lse;         // forward output (fwd) / input (bwd)
+  const void* o_in;   // backward input: the forward's O
+  const void* dout;   // backward input: dO
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;       // backward workspace: rowsum(dO * O), [B, Hq, Sq]
+  int B, Hq, Hkv, Sq, Skv, D;
+  float scale;
+  int causal;
+  const int32_t* kv_lens;  // [B, Hkv] or null
+  attn_dtype_t dtype;
+  unsigned int* err;       // device error word (ATTN_DEVERR_* bits)
+};
+
+// Counts one kernel launch issued by the library (see attn_launch_count()).
+void count_launches(int n);
+
+// CUDA-core kernels (fp32 arithmetic): the fp32 path, any D in {64, 128}.
+cudaError_t simt_fwd(const Problem& p, cudaStream_t stream);
+cudaError_t simt_bwd(const Problem& p, cudaStream_t stream);
+
+// Reads one valid key length on the device: clamps to [0, Skv], flags out-of-range.
+__device__ __forceinline__ int load_kv_len(const int32_t* kv_lens, int b, int kvh, int Hkv,
+                                           int Skv, unsigned int* err) {
+  if (kv_lens == nullptr) return Skv;
+  int L = __ldg(kv_lens + (int64_t)b * Hkv + kvh);
+  if (L < 0 || L > Skv) {
+    if (err != nullptr) atomicOr(err, ATTN_DEVERR_KVLEN);
+    L = L < 0 ? 0 : Skv;
+  }
+  return L;
+}
+
+}  // namespace attn

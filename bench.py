@@ -1,0 +1,461 @@
+#!/usr/bin/env python
+"""Throughput of the fused attention hot path (forward + backward) on one GB300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl ours]
+
+A step is one pass of the whole hot path over one batch of synthetic input: attn_fwd
+then (where the workload has a backward) attn_bwd, both through the C ABI. The value is
+TFLOP/s with the pages' counting rule (4 * B * Hq * Sq * Skv_eff * D for the forward,
+2.5 x that for the backward), inputs already resident in HBM; L2 is flushed (a 512 MiB
+write) before every step, outside the timed events. ``e2e`` is the same metric with the
+inputs copied from pinned host memory and every output copied back, inside the timed
+region. Under torchrun each rank runs an independent replica (attention over
+independent batches and heads needs no exchange); the time is the max over ranks.
+
+``--impl reference`` times the float64 CPU oracle instead, on the host cores, on a
+bounded sample of the same workload per step (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, HERE)
+
+from attention_sm_flash_gb300 import metrics, workloads  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s (bf16) and % of GB300 dense BF16 tensor peak"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+# FP32 FMA peak for the CUDA-core path: 152 SMs x 128 FMA/clk x 2 FLOP x 2.07 GHz
+FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="c2", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work in the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(HERE, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(w, inp):
+    lens = inp["kv_lens"]
+    fwd = metrics.fwd_flops(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.causal, lens)
+    bwd = metrics.bwd_flops(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.causal, lens) if w.has_bwd else 0.0
+    pairs = metrics.visible_pairs(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.causal, lens)
+    cfg = {"workload": f"{w.key} {w.name}", "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq,
+           "Skv": w.Skv, "Skv_eff": round(pairs / (w.B * w.Hq * w.Sq), 2), "D": w.D,
+           "causal": w.causal, "kv_lens": w.lens_kind, "scale": round(w.scale, 6),
+           "step": "attn_fwd + attn_bwd" if w.has_bwd else "attn_fwd",
+           "parallelism": "replicas (independent problem per rank, no collective)"}
+    return cfg, fwd, bwd
+
+
+# ----------------------------------------------------------------------- CPU oracle
+def oracle_sample(w, inp, target_s):
+    """A bounded slice of the workload for the float64 oracle, sized to ~target_s.
+
+    Returns (run, flops, description). Training workloads use whole (batch, kv head)
+    groups, forward + backward; the long-sequence workloads use query rows of head 0.
+    """
+    import oracle
+
+    g = w.Hq // w.Hkv
+    lens = inp["kv_lens"]
+
+    def unit_group(b, kvh):
+        sl = slice(kvh * g, (kvh + 1) * g)
+        q = inp["q"][b:b + 1, :, sl]
+        k = inp["k"][b:b + 1, :, kvh:kvh + 1]
+        v = inp["v"][b:b + 1, :, kvh:kvh + 1]
+        ln = None if lens is None else lens[b:b + 1, kvh:kvh + 1]
+        fl = metrics.fwd_flops(1, g, 1, w.Sq, w.Skv, w.D, w.causal, ln)
+        if w.has_bwd:
+            do = inp["do"][b:b + 1, :, sl]
+            fl *= 3.5
+
+            def run():
+                oracle.forward(q, k, v, w.scale, w.causal, ln)
+                oracle.backward(q, k, v, do, w.scale, w.causal, ln)
+        else:
+            def run():
+                oracle.forward(q, k, v, w.scale, w.causal, ln)
+        return run, fl
+
+    if w.Sq * w.Skv <= 4096 * 4096:
+        units = [(b, kvh) for b in range(w.B) for kvh in range(w.Hkv)]
+        run0, fl0 = unit_group(*units[0])
+        t0 = time.perf_counter()
+        run0()
+        dt = max(time.perf_counter() - t0, 1e-4)
+        n = int(max(1, min(len(units), round(target_s / dt))))
+        runs = [unit_group(*u) for u in units[:n]]
+
+        def run():
+            for r, _ in runs:
+                r()
+        return run, sum(f for _, f in runs), f"{n} of {len(units)} (batch, kv-head) groups, " \
+            f"{'fwd+bwd' if w.has_bwd else 'fwd'}, all query heads of each group"
+    # long sequences: rows of head 0
+    q = inp["q"][0:1, :, 0:1]
+    k = inp["k"][0:1, :, 0:1]
+    v = inp["v"][0:1, :, 0:1]
+    ln = None if lens is None else lens[0:1, 0:1]
+
+    def rows_run(nrows):
+        rows = np.arange(nrows)
+
+        def run():
+            oracle.forward_rows(q, k, v, w.scale, w.causal, ln, 0, 0, rows)
+        L = w.Skv if ln is None else int(ln[0, 0])
+        return run, 4.0 * w.D * nrows * L
+
+    r, _ = rows_run(64)
+    t0 = time.perf_counter()
+    r()
+    dt = max(time.perf_counter() - t0, 1e-4)
+    nrows = int(max(64, min(w.Sq, 64 * target_s / dt)))
+    run, fl = rows_run(nrows)
+    return run, fl, f"{nrows} query rows of (batch 0, head 0), fwd, all valid keys"
+
+
+def cpu_info():
+    cores = len(os.sched_getaffinity(0))
+    threads = None
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max((i.get("num_threads", 0) for i in threadpool_info()), default=None)
+    except Exception:
+        pass
+    return cores, threads
+
+
+def cpu_baseline(w, inp, seconds):
+    run, fl, desc = oracle_sample(w, inp, seconds)
+    t0 = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t0
+    cores, threads = cpu_info()
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads or cores,
+            "host_cores": cores, "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
+
+
+# ------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index, enabled=True):
+        self.index = str(index)
+        self.proc = None
+        self.path = None
+        if not enabled:
+            return
+        try:
+            os.makedirs(os.path.join(HERE, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(HERE, "gpurun_out", f"clocks_rank{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            rows = [[p.strip() for p in line.split(",")] for line in f]
+        rows = [r for r in rows if len(r) >= 9]
+        seen = {r[0] for r in rows}
+        want = self.index if self.index in seen else (seen.pop() if len(seen) == 1 else None)
+        for parts in rows:
+                if parts[0] != want:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- ours
+def traffic_for(kernel_key):
+    """DRAM bytes per launch recorded from an ncu capture of the current sources, or None."""
+    path = os.path.join(HERE, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    from attention_sm_flash_gb300 import build as libbuild
+    stamp = libbuild._stamp(())[:16]
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel_key:
+                if len(parts) >= 4 and parts[3] != stamp:
+                    return None
+                return float(parts[2])
+    return None
+
+
+def run_ours(args, rank, world, local_rank):
+    from attention_sm_flash_gb300 import attn
+    from attention_sm_flash_gb300 import build as libbuild
+
+    if not os.path.exists(attn.LIB_PATH):
+        libbuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = workloads.get(args.workload)
+    inp = workloads.make_inputs(w)
+    cfg, fwd_fl, bwd_fl = workload_config(w, inp)
+    step_fl = fwd_fl + bwd_fl
+    td = w.torch_dtype
+    stream = torch.cuda.current_stream(dev)
+
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    do = inp["do"].to(dev) if w.has_bwd else None
+    lens = inp["kv_lens"].to(dev) if inp["kv_lens"] is not None else None
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    if w.has_bwd:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws_bytes = attn.attn_bwd_workspace_size(w.B, w.Hq, w.Sq, w.D,
+                                                attn.ATTN_BF16 if w.dtype == "bf16" else attn.ATTN_F32)
+        ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.int16, device=dev)  # 512 MiB
+
+    def fwd():
+        attn.attn_fwd(q, k, v, o, lse, w.causal, w.scale, lens, stream)
+
+    def bwd():
+        attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, lens, ws, stream)
+
+    def step_events(n):
+        return [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+
+    def run_steps(evs):
+        for e in evs:
+            flush_buf.zero_()
+            e[0].record(stream)
+            fwd()
+            e[1].record(stream)
+            if w.has_bwd:
+                bwd()
+            e[2].record(stream)
+
+    run_steps(step_events(max(args.warmup, 3)))
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                           os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank],
+                           enabled=not args.no_clocks)
+    # clock pre-roll (untimed): about half a second of steps so clocks settle under load
+    t_end = time.perf_counter() + 0.5
+    while time.perf_counter() < t_end:
+        run_steps(step_events(1))
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    n0 = attn.attn_launch_count()
+    evs = step_events(args.steps)
+    t0 = time.perf_counter()
+    run_steps(evs)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    launches = attn.attn_launch_count() - n0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_ms = [a + b for a, b in zip(fwd_ms, bwd_ms)]
+    ms = statistics.mean(step_ms)
+    ms_all = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(ms_all, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(ms_all.item())
+    value = world * step_fl / (ms_max * 1e-3) / 1e12
+
+    # e2e: the same step through the C ABI from pinned host buffers, outputs copied back
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (inp[n].pin_memory() for n in ("q", "k", "v"))
+        hdo = inp["do"].pin_memory() if w.has_bwd else None
+        hl = inp["kv_lens"].pin_memory() if inp["kv_lens"] is not None else None
+        outs_h = [torch.empty(o.shape, dtype=td).pin_memory(),
+                  torch.empty(lse.shape, dtype=torch.float32).pin_memory()]
+        if w.has_bwd:
+            outs_h += [torch.empty(t.shape, dtype=td).pin_memory() for t in (dq, dk, dv)]
+        outs_d = [o, lse] + ([dq, dk, dv] if w.has_bwd else [])
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, hl) if t is not None)
+        d2h = sum(t.numel() * t.element_size() for t in outs_h)
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            if hdo is not None:
+                do.copy_(hdo, non_blocking=True)
+            if hl is not None:
+                lens.copy_(hl, non_blocking=True)
+            fwd()
+            if w.has_bwd:
+                bwd()
+            for hd, dd in zip(outs_h, outs_d):
+                hd.copy_(dd, non_blocking=True)
+
+        for _ in range(max(args.warmup, 3)):
+            e2e_step()
+        torch.cuda.synchronize()
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_ev.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e_ev.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = s_ev.elapsed_time(e_ev) / args.steps
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        if world > 1:
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+        e2e = {"value": world * step_fl / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    peaks, peak_src = load_peaks()
+    fwd_mean = statistics.mean(fwd_ms)
+    bwd_mean = statistics.mean(bwd_ms) if w.has_bwd else 0.0
+    dom = "attn_bwd" if bwd_mean > fwd_mean else "attn_fwd"
+    dom_fl = bwd_fl if dom == "attn_bwd" else fwd_fl
+    dom_ms = bwd_mean if dom == "attn_bwd" else fwd_mean
+    achieved = dom_fl / (dom_ms * 1e-3) / 1e12
+    if w.dtype == "bf16":
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        bound, peak_note = "tensor", f"bf16 dense burst, {peak_src}"
+    else:
+        peak = FP32_FMA_TFLOPS
+        bound, peak_note = "alu", "FP32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz"
+    roofline = {"bound": bound, "achieved": round(achieved, 3), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic_for(f"{dom}:{w.key}"), "kernel": dom,
+                "peak_source": peak_note,
+                "algorithmic_flops_per_launch": dom_fl}
+    bf16_peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic: seeded N(0,1) inputs with the pages' shapes (no real activations)",
+        "config": dict(cfg, l2="flushed (512 MiB write) before every step, outside the "
+                               "timed events"),
+        "pct_of_bf16_peak": round(100 * value / world / bf16_peak, 2),
+        "peak_source": peak_src,
+        "fwd_tflops": round(fwd_fl / (fwd_mean * 1e-3) / 1e12, 3),
+        "bwd_tflops": round(bwd_fl / (bwd_mean * 1e-3) / 1e12, 3) if w.has_bwd else None,
+        "fwd_ms": round(fwd_mean, 5), "bwd_ms": round(bwd_mean, 5) if w.has_bwd else None,
+        "wall_s_timed": round(wall, 4),
+        "e2e": e2e, "gpu_launches": int(launches), "roofline": roofline,
+        "clocks": clocks, "library": attn.build_info(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------- reference
+def run_reference(args, world):
+    w = workloads.get(args.workload)
+    inp = workloads.make_inputs(w)
+    cfg, _, _ = workload_config(w, inp)
+    budget = 150.0  # seconds for warmup + steps together
+    per_step = max(0.2, min(10.0, budget / max(1, args.steps + args.warmup)))
+    run, fl, desc = oracle_sample(w, inp, per_step)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    value = fl / (ms * 1e-3) / 1e12
+    cores, threads = cpu_info()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded N(0,1) inputs with the pages' shapes",
+        "config": cfg,
+        "cpu_baseline": {"kind": "oracle", "cores": threads or cores, "host_cores": cores,
+                         "sample": desc, "value": value, "unit": "TFLOP/s"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, world)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

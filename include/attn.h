@@ -1,0 +1,136 @@
+/*
+ * attn.h - C ABI of libattn: fused scaled-dot-product attention, forward and backward,
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (forward): for every batch b and query head h, with kv head
+ * kvh = h / (Hq / Hkv) and L = the valid key length of (b, kvh),
+ *
+ *     S    = scale * Q[b, :, h, :] . K[b, :L, kvh, :]^T          (Sq x L)
+ *     S_ij = -inf where causal and j > i + (L - Sq)               (bottom-right aligned)
+ *     O    = softmax_rows(S) . V[b, :L, kvh, :]                  (Sq x D)
+ *     LSE  = log(sum_j exp(S_ij))   (natural log, fp32)
+ *
+ * computed without materialising S: an online softmax over K/V tiles with a running
+ * max and sum ("xtrain evolution.md", infra table row T14: fused flash attention,
+ * online softmax tiled over KV, no N x N scores). Query heads share kv heads in groups
+ * of Hq / Hkv (row T15: true GQA, dst = kvh * group + r). Keys at or past the valid
+ * length are padding and never influence a result ("LingBot full-pipeline analysis
+ * report", section "same-GPU FA2/FA3 hardware comparison": the FP64 reference uses only
+ * the cu_seqlens-valid K/V). A query row with no visible key gets O = 0, LSE = -inf.
+ *
+ * The backward (row T14: recompute the scores, D = sum(dO * O) simplifies the softmax
+ * Jacobian) gives dQ, dK, dV of sum(O * dO); kv-head gradients are the sum over the
+ * query heads of the group in a fixed order (row T15: deterministic in-group sum, no
+ * atomics). Results are bitwise reproducible run to run for identical inputs.
+ *
+ * Layout (all contiguous, row-major, D innermost; the pages' token-major [tokens, H, D]
+ * with a batch dimension in front):
+ *     q, o, dout, dq : [B, Sq,  Hq,  D]
+ *     k, v, dk, dv   : [B, Skv, Hkv, D]
+ *     lse            : [B, Hq, Sq]  fp32
+ *     kv_lens        : [B, Hkv]     int32, device memory, or NULL (= every length Skv)
+ * Element type: ATTN_BF16 (bfloat16) or ATTN_F32 (float) for q, k, v, o, dout, dq, dk,
+ * dv; lse is always fp32; accumulation is always fp32. Outputs are rounded to the
+ * element type with round-to-nearest-even.
+ *
+ * Ownership and streams: every pointer is a device pointer owned by the caller; the
+ * library never allocates, frees or retains one. Calls are asynchronous on `stream`
+ * (NULL = the legacy default stream) and never modify their inputs. The backward needs
+ * a caller-provided device workspace of attn_bwd_workspace_size() bytes.
+ *
+ * Errors: argument checks are synchronous, on the host, before anything is launched;
+ * a failed check returns a negative status and launches nothing. Values that live in
+ * device memory (kv_lens) cannot be checked on the host: the kernels clamp them to
+ * [0, Skv] and record the fact in a device error word, which attn_peek_device_error()
+ * reads. Kernels that wait on barriers bound every wait; a wait that runs out records
+ * ATTN_DEVERR_TIMEOUT and the kernel returns instead of hanging.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (binary-compatible with cudaStream_t / CUstream). */
+typedef struct CUstream_st* attn_stream_t;
+
+typedef enum {
+  ATTN_BF16 = 0, /* bfloat16 inputs and outputs */
+  ATTN_F32 = 1   /* float inputs and outputs */
+} attn_dtype_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = -1, /* a null/misaligned pointer, a bad size, a non-finite scale */
+  ATTN_ERR_UNSUPPORTED = -2, /* a valid request this build does not implement (e.g. D) */
+  ATTN_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed */
+  ATTN_ERR_TIMEOUT = -4,     /* a device-side bounded wait ran out (see the error word) */
+  ATTN_ERR_WORKSPACE = -5    /* the backward workspace is missing or too small */
+} attn_status_t;
+
+/* Bits of the device error word. */
+#define ATTN_DEVERR_KVLEN 0x1u   /* a kv_lens entry was outside [0, Skv]; it was clamped */
+#define ATTN_DEVERR_TIMEOUT 0x2u /* a bounded barrier wait ran out; outputs are invalid */
+
+/*
+ * Forward. q, k, v: inputs; o: output [B, Sq, Hq, D]; lse: output [B, Hq, Sq] fp32.
+ * B, Sq >= 0 (0 = nothing to do); Hq, Hkv >= 1 with Hq % Hkv == 0; Skv >= 0 (0 = every
+ * row empty); D in {64, 128} (else ATTN_ERR_UNSUPPORTED); scale finite; causal 0 or 1.
+ * Pointers to q, k, v, o must be 16-byte aligned; lse and kv_lens 4-byte aligned.
+ */
+ATTN_API attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int Hq, int Hkv, int Sq, int Skv, int D, float scale,
+                       int causal, const int32_t* kv_lens, attn_dtype_t dtype,
+                       attn_stream_t stream);
+
+/*
+ * Backward. q, k, v, o, lse: the forward's inputs and outputs; dout: the gradient of O
+ * [B, Sq, Hq, D]; dq, dk, dv: outputs (dk, dv are zero at keys past the valid length).
+ * The same size, alignment and kv_lens rules as attn_fwd; in addition dout, dq, dk,
+ * dv must be 16-byte aligned and `workspace` must hold at least
+ * attn_bwd_workspace_size(...) bytes of device memory, 256-byte aligned, for the call's
+ * exclusive use until the stream reaches the end of the call (ATTN_ERR_WORKSPACE
+ * otherwise). The workspace holds delta = rowsum(dO * O) [B, Hq, Sq] fp32.
+ */
+ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       int B, int Hq, int Hkv, int Sq, int Skv, int D, float scale,
+                       int causal, const int32_t* kv_lens, attn_dtype_t dtype,
+                       void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/* Bytes of device workspace attn_bwd needs for these sizes (0 for an empty problem). */
+ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Sq, int D, attn_dtype_t dtype);
+
+/*
+ * Waits for `stream`, then reads and clears the current device's error word.
+ * Writes the raw ATTN_DEVERR_* bits to *bits when bits is not NULL. Returns
+ * ATTN_ERR_TIMEOUT if the timeout bit was set, ATTN_ERR_INVALID_ARG if only the
+ * kv_lens bit was set, ATTN_OK if the word was clear, ATTN_ERR_CUDA on a CUDA error.
+ */
+ATTN_API attn_status_t attn_peek_device_error(uint32_t* bits, attn_stream_t stream);
+
+/* A static, human-readable name of a status code. */
+ATTN_API const char* attn_status_string(attn_status_t status);
+
+/* The library's build identity (kernel families compiled in), a static string. */
+ATTN_API const char* attn_build_info(void);
+
+/* The number of kernel launches this library has issued in this process (all devices,
+ * all threads); a monotonically increasing host-side counter. */
+ATTN_API uint64_t attn_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

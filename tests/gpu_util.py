@@ -1,0 +1,104 @@
+"""Helpers for the GPU parity tests: run the library through its C ABI on seeded inputs
+and compare with the float64 oracle element by element."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from attention_sm_flash_gb300 import attn
+
+# Tolerances: |gpu - ref| <= atol + rtol * |ref| on every finite element.
+TOL = {
+    "f32": {"o": (1e-5, 1e-5), "lse": (1e-5, 1e-5), "grad": (1e-5, 1e-5)},
+    "bf16": {"o": (2e-2, 2e-2), "lse": (1e-3, 0.0), "grad": (2e-2, 2e-2)},
+}
+GUARD = 4096  # guard elements on each side of every output buffer
+SENTINEL = 12288.0  # exact in bf16 and fp32
+
+
+def to_dev(x):
+    return None if x is None else x.cuda()
+
+
+def guarded(shape, dtype, fill=float("nan")):
+    """An output tensor inside a larger buffer whose guard bands hold a sentinel."""
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * GUARD,), SENTINEL, dtype=dtype, device="cuda")
+    # keep the view 16-byte aligned: GUARD elements of >= 2 bytes is a multiple of 16
+    view = buf[GUARD:GUARD + n].view(shape)
+    view.fill_(fill)
+    return buf, view
+
+
+def check_guard(buf, name):
+    lo = buf[:GUARD].float().cpu()
+    hi = buf[-GUARD:].float().cpu()
+    assert torch.all(lo == SENTINEL) and torch.all(hi == SENTINEL), f"{name}: guard band written"
+
+
+def compare(name, got, ref, atol, rtol, report=None):
+    """Element-wise tolerance check; -inf positions must agree exactly; no NaN allowed."""
+    g = got.detach().double().cpu().numpy() if hasattr(got, "detach") else np.asarray(got)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert g.shape == ref.shape, (name, g.shape, ref.shape)
+    assert not np.isnan(g).any(), f"{name}: NaN in output"
+    ninf_ref = np.isneginf(ref)
+    assert np.array_equal(np.isneginf(g), ninf_ref), f"{name}: -inf pattern differs"
+    fin = np.isfinite(ref)
+    diff = np.abs(g[fin] - ref[fin])
+    bound = atol + rtol * np.abs(ref[fin])
+    bad = diff > bound
+    rel_l2 = float(np.linalg.norm(g[fin] - ref[fin]) / max(np.linalg.norm(ref[fin]), 1e-300))
+    if report is not None:
+        report[name] = {"max_abs": float(diff.max()) if diff.size else 0.0, "rel_l2": rel_l2}
+    if bad.any():
+        idx = np.argmax(diff - bound)
+        raise AssertionError(f"{name}: {int(bad.sum())} of {bad.size} elements out of "
+                             f"tolerance; worst |d|={diff[idx]:.3e} ref={ref[fin][idx]:.4e} "
+                             f"bound={bound[idx]:.3e}; rel_l2={rel_l2:.3e}")
+    return rel_l2
+
+
+def run_fwd(inp, w, guard=True):
+    q, k, v = to_dev(inp["q"]), to_dev(inp["k"]), to_dev(inp["v"])
+    lens = to_dev(inp["kv_lens"])
+    B, Sq, Hq, D = q.shape
+    if guard:
+        obuf, o = guarded(q.shape, q.dtype)
+        lbuf, lse = guarded((B, Hq, Sq), torch.float32)
+    else:
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full((B, Hq, Sq), float("nan"), device="cuda")
+    attn.attn_fwd(q, k, v, o, lse, causal=w.causal, scale=w.scale, kv_lens=lens)
+    torch.cuda.synchronize()
+    st, bits = attn.attn_peek_device_error()
+    assert st == attn.ATTN_OK, (st, bits)
+    if guard:
+        check_guard(obuf, "o")
+        check_guard(lbuf, "lse")
+    return o, lse
+
+
+def run_bwd(inp, w, o, lse, guard=True):
+    q, k, v = to_dev(inp["q"]), to_dev(inp["k"]), to_dev(inp["v"])
+    do = to_dev(inp["do"])
+    lens = to_dev(inp["kv_lens"])
+    bufs = []
+    outs = []
+    for t in (q, k, v):
+        if guard:
+            b, x = guarded(t.shape, t.dtype)
+            bufs.append(b)
+        else:
+            x = torch.full_like(t, float("nan"))
+        outs.append(x)
+    dq, dk, dv = outs
+    attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal=w.causal, scale=w.scale,
+                  kv_lens=lens)
+    torch.cuda.synchronize()
+    st, bits = attn.attn_peek_device_error()
+    assert st == attn.ATTN_OK, (st, bits)
+    for b, n in zip(bufs, ("dq", "dk", "dv")):
+        check_guard(b, n)
+    return dq, dk, dv

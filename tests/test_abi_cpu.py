@@ -1,0 +1,115 @@
+"""The C-ABI library loads and exports every symbol include/attn.h declares, and its
+host-side argument checks reject bad calls before touching CUDA (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_sm_flash_gb300 import attn
+from attention_sm_flash_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return attn.load()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "attn.h")) as f:
+        text = f.read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(attn.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_build_info(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert attn.status_string(code).startswith("ATTN_")
+    assert "sm_103a" in attn.build_info()
+
+
+def test_workspace_size(lib):
+    n = attn.attn_bwd_workspace_size(4, 8, 2048, 128, attn.ATTN_BF16)
+    assert n >= 4 * 8 * 2048 * 4 and n % 256 == 0
+    assert attn.attn_bwd_workspace_size(0, 8, 2048, 128, attn.ATTN_BF16) == 0
+
+
+A = 0x10000  # a fake, 256-byte aligned "device address": never dereferenced here
+
+
+def fwd(lib, **kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, Hq=2, Hkv=2, Sq=8, Skv=8, D=64, scale=0.125,
+                causal=0, kv_lens=None, dtype=attn.ATTN_BF16, stream=None)
+    args.update(kw)
+    return lib.attn_fwd(*args.values())
+
+
+def bwd(lib, **kw):
+    args = dict(q=A, k=A, v=A, o=A, do=A, lse=A, dq=A, dk=A, dv=A, B=1, Hq=2, Hkv=2, Sq=8,
+                Skv=8, D=64, scale=0.125, causal=0, kv_lens=None, dtype=attn.ATTN_BF16,
+                ws=A, ws_bytes=1 << 20, stream=None)
+    args.update(kw)
+    return lib.attn_bwd(*args.values())
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(Hq=3, Hkv=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Hkv=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Sq=-5), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Skv=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(D=256), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(causal=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=7), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(o=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(lse=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q=A + 8), attn.ATTN_ERR_INVALID_ARG),
+    (dict(k=A + 2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(lse=A + 2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(kv_lens=A + 1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=70000, Hkv=1), attn.ATTN_ERR_UNSUPPORTED),
+])
+def test_fwd_rejects_bad_arguments(lib, kw, want):
+    assert fwd(lib, **kw) == want
+
+
+def test_empty_problems_are_a_no_op(lib):
+    assert fwd(lib, B=0) == attn.ATTN_OK
+    assert fwd(lib, Sq=0, q=None, o=None, lse=None) == attn.ATTN_OK
+    assert bwd(lib, B=0) == attn.ATTN_OK
+    assert bwd(lib, Sq=0, Skv=0) == attn.ATTN_OK
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(ws=None), attn.ATTN_ERR_WORKSPACE),
+    (dict(ws_bytes=100), attn.ATTN_ERR_WORKSPACE),
+    (dict(ws=A + 16), attn.ATTN_ERR_WORKSPACE),
+    (dict(dq=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(do=A + 4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dv=A + 4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=4, Hkv=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=32), attn.ATTN_ERR_UNSUPPORTED),
+])
+def test_bwd_rejects_bad_arguments(lib, kw, want):
+    assert bwd(lib, **kw) == want
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        attn.attn_fwd(q, q, q, q.clone(), torch.zeros(1, 2, 8))
