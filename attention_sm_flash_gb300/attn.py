@@ -29,7 +29,8 @@ ATTN_DEVERR_KVLEN = 0x1
 ATTN_DEVERR_TIMEOUT = 0x2
 
 EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_peek_device_error",
-            "attn_status_string", "attn_build_info", "attn_launch_count")
+            "attn_status_string", "attn_build_info", "attn_launch_count", "attn_bwd_noalloc")
+ATTN_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _lib = None
 
@@ -64,6 +65,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_build_info.restype = ctypes.c_char_p
     lib.attn_build_info.argtypes = []
     lib.attn_launch_count.restype = ctypes.c_uint64
+    lib.attn_bwd_noalloc.restype = i
+    lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i,
+                                     vp, i, vp]
     lib.attn_launch_count.argtypes = []
     _lib = lib
     return lib
@@ -153,6 +157,23 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal: bool = False,
                          workspace.numel(), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
+
+
+def attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, causal: bool = False,
+                     scale: float | None = None, kv_lens=None, stream=None) -> None:
+    """attn_bwd without a workspace, for callers that cannot allocate device memory: the
+    scratch lives in a fixed-size array inside the library (see include/attn.h)."""
+    _check_cuda(q, k, v, o, dout, lse, dq, dk, dv, kv_lens)
+    B, Sq, Hq, D = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    st = load().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Skv, D,
+                                 float(scale), int(bool(causal)), _ptr(kv_lens), _dtype_code(q),
+                                 _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_noalloc")
 
 
 def attn_peek_device_error(stream=None) -> tuple[int, int]:

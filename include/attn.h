@@ -111,6 +111,43 @@ ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, con
 /* Bytes of device workspace attn_bwd needs for these sizes (0 for an empty problem). */
 ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Sq, int D, attn_dtype_t dtype);
 
+/* Size of the library's static device scratch array used by attn_bwd_noalloc: 8 MiB,
+ * enough for B * Hq * Sq <= 2,097,152 query rows. */
+#define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * attn_bwd_noalloc - the backward for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for integration only.
+ *
+ * Some callers have no way to obtain device scratch at call time: a host that has
+ * reserved all device memory for its own pool and hands an operator only its input and
+ * output buffers, or a latency-critical loop that must not call cudaMalloc/cudaFree
+ * because those calls can synchronize the device and stall other streams. This entry
+ * point takes the same arguments as attn_bwd minus the workspace and uses a scratch
+ * array that lives in the library itself (a static __device__ array of
+ * ATTN_NOALLOC_SCRATCH_BYTES, held on every GPU that loads the library until the process
+ * exits). It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * - Size limit: when attn_bwd_workspace_size() for these sizes exceeds
+ *   ATTN_NOALLOC_SCRATCH_BYTES it returns ATTN_ERR_WORKSPACE and launches nothing.
+ * - Set-up: the first call on a device looks up the array's device address with that
+ *   device current (cudaGetSymbolAddress); make that first call before any stream
+ *   capture begins.
+ * - Sharing: every call on a device uses the same array, which keeps whatever the last
+ *   call left in it. Each call rewrites all the scratch it reads (delta), so nothing has
+ *   to start at zero. Calls whose GPU work can overlap (different streams, or threads
+ *   without ordering between them) race on the array and produce wrong gradients: issue
+ *   them on one stream, or order them with events.
+ * Everything else (arguments, layout, results, errors) is as for attn_bwd, whose code
+ * path it runs.
+ */
+ATTN_API attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v,
+                                        const void* o, const void* dout, const float* lse,
+                                        void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                                        int Sq, int Skv, int D, float scale, int causal,
+                                        const int32_t* kv_lens, attn_dtype_t dtype,
+                                        attn_stream_t stream);
+
 /*
  * Waits for `stream`, then reads and clears the current device's error word.
  * Writes the raw ATTN_DEVERR_* bits to *bits when bits is not NULL. Returns

@@ -113,3 +113,10 @@ def test_binding_refuses_cpu_tensors(lib):
     q = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         attn.attn_fwd(q, q, q, q.clone(), torch.zeros(1, 2, 8))
+
+
+def test_noalloc_rejects_oversize_before_touching_cuda(lib):
+    rows = attn.ATTN_NOALLOC_SCRATCH_BYTES // 4 + 64
+    st = lib.attn_bwd_noalloc(A, A, A, A, A, A, A, A, A, 1, 1, 1, rows, 16, 64, 0.125, 0,
+                              None, attn.ATTN_BF16, None)
+    assert st == attn.ATTN_ERR_WORKSPACE
