@@ -222,6 +222,20 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+# --------------------------------------------------------------------- replicas
+def reduce_max(x: float, device) -> float:
+    """The max of a per-rank scalar over all ranks (the identity without a process group)."""
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step: float, ms_max: float, world: int) -> float:
+    """Whole-job throughput: every rank's work over the slowest rank's step time."""
+    return world * flops_per_rank_step / (ms_max * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------------------- ours
 def traffic_for(kernel_key):
     """DRAM bytes per launch recorded from an ncu capture of the current sources, or None."""
@@ -313,11 +327,8 @@ def run_ours(args, rank, world, local_rank):
     bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     step_ms = [a + b for a, b in zip(fwd_ms, bwd_ms)]
     ms = statistics.mean(step_ms)
-    ms_all = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(ms_all, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(ms_all.item())
-    value = world * step_fl / (ms_max * 1e-3) / 1e12
+    ms_max = reduce_max(ms, dev)
+    value = whole_job_tflops(step_fl, ms_max, world)
 
     # e2e: the same step through the C ABI from pinned host buffers, outputs copied back
     e2e = None
@@ -356,12 +367,8 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
         e_ev.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = s_ev.elapsed_time(e_ev) / args.steps
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        if world > 1:
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-        e2e = {"value": world * step_fl / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e_ms = reduce_max(s_ev.elapsed_time(e_ev) / args.steps, dev)
+        e2e = {"value": whole_job_tflops(step_fl, e2e_ms, world), "unit": "TFLOP/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h)}
 
