@@ -29,7 +29,8 @@ ATTN_DEVERR_KVLEN = 0x1
 ATTN_DEVERR_TIMEOUT = 0x2
 
 EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_peek_device_error",
-            "attn_status_string", "attn_build_info", "attn_launch_count", "attn_bwd_noalloc")
+            "attn_status_string", "attn_build_info", "attn_launch_count", "attn_bwd_noalloc",
+            "attn_test_inject_fault", "attn_last_cuda_error")
 ATTN_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _lib = None
@@ -38,7 +39,10 @@ _lib = None
 class AttnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {status_string(status)} ({status})")
+        extra = ""
+        if status == ATTN_ERR_CUDA:
+            extra = ": " + load().attn_last_cuda_error().decode()
+        super().__init__(f"{what}: {status_string(status)} ({status}){extra}")
 
 
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -64,7 +68,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_status_string.argtypes = [i]
     lib.attn_build_info.restype = ctypes.c_char_p
     lib.attn_build_info.argtypes = []
+    lib.attn_last_cuda_error.restype = ctypes.c_char_p
+    lib.attn_last_cuda_error.argtypes = []
     lib.attn_launch_count.restype = ctypes.c_uint64
+    lib.attn_test_inject_fault.restype = None
+    lib.attn_test_inject_fault.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
     lib.attn_bwd_noalloc.restype = i
     lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i,
                                      vp, i, vp]
@@ -84,6 +92,11 @@ def build_info() -> str:
 def attn_launch_count() -> int:
     """Kernel launches the library has issued in this process."""
     return int(load().attn_launch_count())
+
+
+def attn_test_inject_fault(mask: int, timeout_ms: int = 0) -> None:
+    """Test-only: the next bf16 forward launch injects a fault (see include/attn.h)."""
+    load().attn_test_inject_fault(int(mask), int(timeout_ms))
 
 
 def _ptr(t):

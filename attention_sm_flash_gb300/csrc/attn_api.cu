@@ -57,7 +57,13 @@ attn_status_t check_common(int B, int Hq, int Hkv, int Sq, int Skv, int D, float
   return ATTN_OK;
 }
 
-attn_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+attn_status_t from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return ATTN_OK;
+  g_last_cuda = e;
+  return ATTN_ERR_CUDA;
+}
 
 std::atomic<uint64_t> g_launches{0};
 
@@ -86,9 +92,9 @@ extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, v
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.D = D;
   p.scale = scale; p.causal = causal; p.kv_lens = kv_lens; p.dtype = dtype;
   cudaError_t e = error_word(&p.err);
-  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  if (e != cudaSuccess) return from_cuda(e);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return from_cuda(simt_fwd(p, s));
+  return from_cuda(dtype == ATTN_BF16 ? tc_fwd(p, s) : simt_fwd(p, s));
 }
 
 extern "C" size_t attn_bwd_workspace_size(int B, int Hq, int Sq, int D, attn_dtype_t dtype) {
@@ -135,9 +141,9 @@ extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, c
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.D = D;
   p.scale = scale; p.causal = causal; p.kv_lens = kv_lens; p.dtype = dtype;
   cudaError_t e = error_word(&p.err);
-  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  if (e != cudaSuccess) return from_cuda(e);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return from_cuda(simt_bwd(p, s));
+  return from_cuda(dtype == ATTN_BF16 ? tc_bwd(p, s) : simt_bwd(p, s));
 }
 
 extern "C" attn_status_t attn_peek_device_error(uint32_t* bits, attn_stream_t stream) {
@@ -168,8 +174,16 @@ extern "C" const char* attn_status_string(attn_status_t status) {
   return "unknown attn status";
 }
 
+extern "C" void attn_test_inject_fault(uint32_t mask, uint32_t timeout_ms) {
+  tc_set_test_fault(mask, (uint64_t)timeout_ms * 1000000ull);
+}
+
+extern "C" const char* attn_last_cuda_error(void) {
+  return g_last_cuda == cudaSuccess ? "no CUDA error" : cudaGetErrorString(g_last_cuda);
+}
+
 extern "C" uint64_t attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 extern "C" const char* attn_build_info(void) {
-  return "libattn sm_103a: simt-fp32 fwd/bwd";
+  return "libattn sm_103a: bf16 fwd+bwd tcgen05/TMA/TMEM; fp32 fwd/bwd CUDA-core";
 }

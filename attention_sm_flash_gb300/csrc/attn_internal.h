@@ -1,6 +1,7 @@
 // Internal interface between the C ABI (attn_api.cu) and the kernel families.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -35,6 +36,19 @@ void count_launches(int n);
 // CUDA-core kernels (fp32 arithmetic): the fp32 path, any D in {64, 128}.
 cudaError_t simt_fwd(const Problem& p, cudaStream_t stream);
 cudaError_t simt_bwd(const Problem& p, cudaStream_t stream);
+// delta = rowsum(dO * O) into p.delta (one warp per row); used by both backward paths.
+cudaError_t simt_delta(const Problem& p, cudaStream_t stream);
+
+// Tensor-core (tcgen05) kernels for bf16, sm_103a.
+cudaError_t tc_fwd(const Problem& p, cudaStream_t stream);
+cudaError_t tc_bwd(const Problem& p, cudaStream_t stream);
+
+// A bf16 [B, S, H, D] tensor as a 4-D TMA map (D, H, S, B) whose box is one head:
+// 64 columns (128 bytes, 128-byte swizzle) x `rows` tokens. False if encoding fails.
+bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int H, int D, int rows);
+// Test-only: the next tensor-core forward launch injects `mask` faults and uses a
+// barrier-wait limit of `timeout_ns` (0 = the default).
+void tc_set_test_fault(uint32_t mask, uint64_t timeout_ns);
 
 // Reads one valid key length on the device: clamps to [0, Skv], flags out-of-range.
 __device__ __forceinline__ int load_kv_len(const int32_t* kv_lens, int b, int kvh, int Hkv,

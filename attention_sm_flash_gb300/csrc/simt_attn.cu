@@ -323,7 +323,20 @@ cudaError_t bwd_launch(const Problem& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <typename T, int D>
+cudaError_t delta_launch(const Problem& p, cudaStream_t s) {
+  const int64_t rows = (int64_t)p.B * p.Sq * p.Hq;
+  simt_delta_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t simt_delta(const Problem& p, cudaStream_t s) {
+  if (p.dtype == ATTN_F32) return p.D == 64 ? delta_launch<float, 64>(p, s) : delta_launch<float, 128>(p, s);
+  return p.D == 64 ? delta_launch<__nv_bfloat16, 64>(p, s) : delta_launch<__nv_bfloat16, 128>(p, s);
+}
 
 cudaError_t simt_fwd(const Problem& p, cudaStream_t s) {
   if (p.dtype == ATTN_F32) return p.D == 64 ? fwd_launch<float, 64>(p, s) : fwd_launch<float, 128>(p, s);

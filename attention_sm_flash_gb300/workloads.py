@@ -86,6 +86,12 @@ WORKLOADS = {
                     lens_lo=1560, lens_hi=32760),
     "c5": Workload("c5", "dit_cross_sq32760_skv512_valid300_h40_d128", 1, 40, 40, 32760, 512,
                    128, "bf16", False, 20265, lens_kind="fixed", lens_fixed=300),
+    # profiling cases: the same kernels at sizes an ncu capture replays quickly, with
+    # inputs still larger than L2 (129 MB)
+    "p_self": Workload("p_self", "profile_self_s16384_h16_d128", 1, 16, 16, 16384, 16384, 128,
+                       "bf16", False, 20266, qk_factor=0.5),
+    "p_train": Workload("p_train", "profile_train_b8_h16_s2048_d128_causal", 8, 16, 4, 2048,
+                        2048, 128, "bf16", True, 20267, has_bwd=True),
 }
 
 

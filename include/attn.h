@@ -156,11 +156,25 @@ ATTN_API attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void
  */
 ATTN_API attn_status_t attn_peek_device_error(uint32_t* bits, attn_stream_t stream);
 
+/* The CUDA runtime's description of the last CUDA error behind an ATTN_ERR_CUDA
+ * returned to the calling thread ("no CUDA error" if none); a static string. */
+ATTN_API const char* attn_last_cuda_error(void);
+
 /* A static, human-readable name of a status code. */
 ATTN_API const char* attn_status_string(attn_status_t status);
 
 /* The library's build identity (kernel families compiled in), a static string. */
 ATTN_API const char* attn_build_info(void);
+
+/*
+ * Test-only fault injection: the next bf16 forward launch applies `mask` (bit 0: its
+ * producer skips its first K tile load, so the consumer's bounded wait runs out) and
+ * gives up a barrier wait after `timeout_ms` (0 = the default of 4 s). The kernel then
+ * records ATTN_DEVERR_TIMEOUT, lets its in-flight copies and MMAs finish, frees its
+ * tensor memory and returns; attn_peek_device_error() reports ATTN_ERR_TIMEOUT. Not for
+ * production use: the outputs of that call are invalid.
+ */
+ATTN_API void attn_test_inject_fault(uint32_t mask, uint32_t timeout_ms);
 
 /* The number of kernel launches this library has issued in this process (all devices,
  * all threads); a monotonically increasing host-side counter. */

@@ -169,3 +169,21 @@ def test_non_default_stream(dt):
     o_ref, lse_ref = oracle.forward(inp["q"], inp["k"], inp["v"], w.scale, True)
     compare("o", o, o_ref, *TOL[dt]["o"])
     compare("lse", lse, lse_ref, *TOL[dt]["lse"])
+
+
+def test_bounded_wait_runs_out_reports_timeout_and_gpu_stays_usable():
+    """A forward whose producer skips one load (test-only injection): the consumer's
+    bounded wait runs out, the kernel records a timeout and returns, and the next call
+    on the same context is correct."""
+    w, inp = case("bf16", B=1, Hq=2, Hkv=2, Sq=256, Skv=256, D=128)
+    q, k, v = inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda()
+    torch.cuda.synchronize()
+    attn.attn_peek_device_error()
+    attn.attn_test_inject_fault(1, 200)
+    attn.forward(q, k, v, scale=w.scale)
+    st, bits = attn.attn_peek_device_error()
+    assert st == attn.ATTN_ERR_TIMEOUT and bits & attn.ATTN_DEVERR_TIMEOUT
+    o, lse = run_fwd(inp, w)
+    o_ref, lse_ref = oracle.forward(inp["q"], inp["k"], inp["v"], w.scale, False)
+    compare("o_after_timeout", o, o_ref, *TOL["bf16"]["o"])
+    compare("lse_after_timeout", lse, lse_ref, *TOL["bf16"]["lse"])
