@@ -7,13 +7,13 @@
 // are padding and never enter a result ("LingBot full-pipeline analysis report", section
 // "same-GPU FA2/FA3 hardware comparison").
 //
-// One persistent CTA per SM (320 threads) loops over work items of 256 query rows of one
+// One persistent CTA per SM (384 threads) loops over work items of 256 query rows of one
 // (batch, head), taken in a longest-first order:
 //   warp 0      TMA producer: a ring of Q tiles (the next item's Q is prefetched), and a
 //               ring of K/V tiles of 128 keys;
 //   warp 1      MMA issuer (one thread): S_t = Q_t K^T into TMEM, O_t += P_t V from TMEM;
-//   warps 2-5   softmax of Q tile 0 (128 rows, one row per thread);
-//   warps 6-9   softmax of Q tile 1.
+//   warps 4-7   softmax of Q tile 0 (128 rows, one row per thread);
+//   warps 8-11  softmax of Q tile 1.
 // TMEM (512 columns): S0 | S1 | O0 | O1. The softmax reads its S row, writes P (bf16)
 // over the first half of the same columns, and the PV MMA reads P from there. A row's
 // running max is only raised (and O, l rescaled) when it grows by more than 2^8, which
@@ -41,7 +41,14 @@ using namespace sm103;
 constexpr int kBM = 128;         // rows of a Q tile (TMEM lanes)
 constexpr int kBN = 128;         // keys of a K/V tile
 constexpr int kItemRows = 2 * kBM;
-constexpr int kThreads = 320;    // warps 0-1: producer, MMA; warps 2-5, 6-9: softmax
+constexpr int kThreads = 384;    // warps 0-3: producer, MMA, 2 idle; 4-7, 8-11: softmax
+// Register split (setmaxnreg): the block launches with kLaunchRegs a thread; warpgroup 0
+// then drops to kRegsLow and the two softmax warpgroups rise to kRegsHigh. The raise
+// draws on the registers the block was launched with, so the split must fit in them.
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsLow = 80;
+constexpr int kRegsHigh = 208;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs, "register split");
 constexpr int kMaxSortedHeads = 64;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows > 2^8
 
@@ -147,8 +154,8 @@ __device__ __forceinline__ int pv_steps(int j, int L) {
 }
 
 template <int D, int NQ, int NST>
-// 10 warps put 3 warps on two of the 4 sub-partitions (16K registers each): <= 168
-// registers per thread.
+// 12 warps, 3 per sub-partition (16K registers each): launched with <= 168 registers a
+// thread, then rebalanced with setmaxnreg (see kRegsLow / kRegsHigh).
 __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
   constexpr int kQTile = kBM * D * 2;     // bytes of a Q tile
   constexpr int kKVTile = kBN * D * 2;    // bytes of a K or V tile
@@ -222,162 +229,167 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
   const uint32_t tmem = c.tmem_base;
   WaitCtl wc{&c.abort, p.err, p.timeout_ns};
 
-  if (warp == 0) {
-    // ------------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      tma_prefetch_map(&p.tm_q);
-      tma_prefetch_map(&p.tm_k);
-      tma_prefetch_map(&p.tm_v);
-    }
-    uint32_t slot = 0, ring_par = 0, qs = 0, q_par = 0;
-    uint32_t issued = 0, last_par = 0;    // per K/V slot: a load was issued / its parity
-    uint32_t q_issued = 0, q_last = 0;    // per Q slot
-    bool ok = true, first = true;
-    for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-      const Item it = decode_item(idx, p, c);
-      if (it.nload == 0) continue;
-      for (int t = 0; t < 2; ++t) {
-        if (!wait_phase_warp(&c.q_empty[qs], q_par ^ 1, wc)) { ok = false; break; }
-        if (lane == 0) {
-          mbar_expect_tx(&c.q_full[qs], kQTile);
-          for (int ch = 0; ch < kChunks; ++ch)
-            tma_load_4d(sQ + qs * kQTile + ch * kQChunk, &p.tm_q, &c.q_full[qs], ch * 64, it.h,
-                        it.q0 + t * kBM, it.b);
-        }
-        q_issued |= 1u << qs;
-        q_last = (q_last & ~(1u << qs)) | (q_par << qs);
-        if (++qs == NQ) { qs = 0; q_par ^= 1; }
+  if (warp < 4) {
+    // warpgroup 0 hands registers to the softmax warpgroups
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsLow) : "memory");
+    if (warp == 0) {
+      // ------------------------------------------------------------- TMA producer
+      if (lane == 0) {
+        tma_prefetch_map(&p.tm_q);
+        tma_prefetch_map(&p.tm_k);
+        tma_prefetch_map(&p.tm_v);
       }
-      for (int j = 0; ok && j < it.nload; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          if (!wait_phase_warp(&c.kv_empty[slot], ring_par ^ 1, wc)) { ok = false; break; }
-          const bool skip = (p.fault & 1u) && blockIdx.x == 0 && first && j == 0 && kv == 0;
-          if (!skip) {
-            if (lane == 0) {
-              mbar_expect_tx(&c.kv_full[slot], kKVTile);
-              for (int ch = 0; ch < kChunks; ++ch)
-                tma_load_4d(sKV + slot * kKVTile + ch * kKVChunk, kv == 0 ? &p.tm_k : &p.tm_v,
-                            &c.kv_full[slot], ch * 64, it.kvh, j * kBN, it.b);
-            }
-            issued |= 1u << slot;
-            last_par = (last_par & ~(1u << slot)) | (ring_par << slot);
-          }
-          if (kv == 1 && needs_fix(j, it.L, p.Skv)) {
-            // zero the padding rows of this V tile once it has landed
-            if (!wait_phase_warp(&c.kv_full[slot], ring_par, wc)) { ok = false; break; }
-            const int r0 = it.L - j * kBN;  // first padding row (>= 1: tile j holds valid keys)
-            const int units = (kBN - r0) * kChunks * 8;
-            uint8_t* base = sKV + slot * kKVTile;
-            for (int e = lane; e < units; e += 32) {
-              const int r = r0 + e / (kChunks * 8);
-              const int rest = e % (kChunks * 8);
-              *reinterpret_cast<uint4*>(base + (rest / 8) * kKVChunk + r * 128 + (rest % 8) * 16) =
-                  make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&c.kv_fixed[slot]);
-          }
-          if (++slot == NST) { slot = 0; ring_par ^= 1; }
-        }
-      }
-      first = false;
-    }
-    // every copy this CTA started lands before its shared memory can go away (after an
-    // abort the consumers may never have waited for them)
-    for (int s = 0; s < NST; ++s)
-      if (issued & (1u << s)) wait_phase_teardown(&c.kv_full[s], (last_par >> s) & 1, 200000000ull);
-    for (int s = 0; s < NQ; ++s)
-      if (q_issued & (1u << s)) wait_phase_teardown(&c.q_full[s], (q_last >> s) & 1, 200000000ull);
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
-      uint32_t slot = 0, ring_par = 0, qs = 0, q_par = 0, fix_par = 0;
-      uint32_t pv0 = 0, pv1 = 0, pc0 = 0, pc1 = 0, ic0 = 0, ic1 = 0;  // per Q tile counters
-      bool ok = true;
+      uint32_t slot = 0, ring_par = 0, qs = 0, q_par = 0;
+      uint32_t issued = 0, last_par = 0;    // per K/V slot: a load was issued / its parity
+      uint32_t q_issued = 0, q_last = 0;    // per Q slot
+      bool ok = true, first = true;
       for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
         const Item it = decode_item(idx, p, c);
         if (it.nload == 0) continue;
-        uint32_t qslot[2];
-#pragma unroll
         for (int t = 0; t < 2; ++t) {
-          qslot[t] = qs;
-          if (!wait_phase(&c.q_full[qs], q_par, wc)) ok = false;
+          if (!wait_phase_warp(&c.q_empty[qs], q_par ^ 1, wc)) { ok = false; break; }
+          if (lane == 0) {
+            mbar_expect_tx(&c.q_full[qs], kQTile);
+            for (int ch = 0; ch < kChunks; ++ch)
+              tma_load_4d(sQ + qs * kQTile + ch * kQChunk, &p.tm_q, &c.q_full[qs], ch * 64, it.h,
+                          it.q0 + t * kBM, it.b);
+          }
+          q_issued |= 1u << qs;
+          q_last = (q_last & ~(1u << qs)) | (q_par << qs);
           if (++qs == NQ) { qs = 0; q_par ^= 1; }
         }
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (it.n[t] == 0) mma_commit(&c.q_empty[qslot[t]]);  // never read: free at once
         for (int j = 0; ok && j < it.nload; ++j) {
-          // S_t = Q_t K_j^T
-          if (!wait_phase(&c.kv_full[slot], ring_par, wc)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (j >= it.n[t]) continue;
-            const uint32_t pv = t == 0 ? pv0 : pv1;
-            // S_t's columns hold P_t(j-1) until that PV product completes
-            if (pv > 0 && !wait_phase(&c.o_done[t], (pv - 1) & 1, wc)) { ok = false; break; }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk / 4) * kQChunk + (kk % 4) * 32;
-              const uint64_t a = smem_desc_sw128(sQa + qslot[t] * kQTile + off, 16, 1024);
-              const uint64_t b = smem_desc_sw128(sKVa + slot * kKVTile + (kk / 4) * kKVChunk + (kk % 4) * 32, 16, 1024);
-              mma_ss(tmem + t * 128, a, b, kIdescS, kk > 0 ? 1u : 0u);
+          for (int kv = 0; kv < 2; ++kv) {
+            if (!wait_phase_warp(&c.kv_empty[slot], ring_par ^ 1, wc)) { ok = false; break; }
+            const bool skip = (p.fault & 1u) && blockIdx.x == 0 && first && j == 0 && kv == 0;
+            if (!skip) {
+              if (lane == 0) {
+                mbar_expect_tx(&c.kv_full[slot], kKVTile);
+                for (int ch = 0; ch < kChunks; ++ch)
+                  tma_load_4d(sKV + slot * kKVTile + ch * kKVChunk, kv == 0 ? &p.tm_k : &p.tm_v,
+                              &c.kv_full[slot], ch * 64, it.kvh, j * kBN, it.b);
+              }
+              issued |= 1u << slot;
+              last_par = (last_par & ~(1u << slot)) | (ring_par << slot);
             }
-            mma_commit(&c.s_full[t]);
-            if (j == it.n[t] - 1) mma_commit(&c.q_empty[qslot[t]]);  // last read of Q_t
-          }
-          if (!ok) break;
-          mma_commit(&c.kv_empty[slot]);
-          if (++slot == NST) { slot = 0; ring_par ^= 1; }
-          // O_t += P_t V_j
-          if (needs_fix(j, it.L, p.Skv)) {
-            if (!wait_phase(&c.kv_fixed[slot], (fix_par >> slot) & 1, wc)) { ok = false; break; }
-            fix_par ^= 1u << slot;
-          } else if (!wait_phase(&c.kv_full[slot], ring_par, wc)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const int steps = pv_steps(j, it.L);
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (j >= it.n[t]) continue;
-            const uint32_t pc = t == 0 ? pc0 : pc1;
-            if (!wait_phase(&c.p_full[t], pc & 1, wc)) { ok = false; break; }
-            if (t == 0) ++pc0; else ++pc1;
-            const uint32_t ic = t == 0 ? ic0 : ic1;
-            if (j == 0 && !wait_phase(&c.o_free[t], (ic & 1) ^ 1, wc)) { ok = false; break; }
-            tc_fence_after();
-            for (int kk = 0; kk < steps; ++kk) {
-              const uint64_t b = smem_desc_sw128(sKVa + slot * kKVTile + kk * 16 * 128, kKVChunk, 1024);
-              mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, b, kIdescPV,
-                     (j > 0 || kk > 0) ? 1u : 0u);
+            if (kv == 1 && needs_fix(j, it.L, p.Skv)) {
+              // zero the padding rows of this V tile once it has landed
+              if (!wait_phase_warp(&c.kv_full[slot], ring_par, wc)) { ok = false; break; }
+              const int r0 = it.L - j * kBN;  // first padding row (>= 1: tile j holds valid keys)
+              const int units = (kBN - r0) * kChunks * 8;
+              uint8_t* base = sKV + slot * kKVTile;
+              for (int e = lane; e < units; e += 32) {
+                const int r = r0 + e / (kChunks * 8);
+                const int rest = e % (kChunks * 8);
+                *reinterpret_cast<uint4*>(base + (rest / 8) * kKVChunk + r * 128 + (rest % 8) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&c.kv_fixed[slot]);
             }
-            mma_commit(&c.o_done[t]);
-            if (t == 0) ++pv0; else ++pv1;
+            if (++slot == NST) { slot = 0; ring_par ^= 1; }
           }
-          if (!ok) break;
-          mma_commit(&c.kv_empty[slot]);
-          if (++slot == NST) { slot = 0; ring_par ^= 1; }
         }
-        if (!ok) break;
-        if (it.n[0] > 0) ++ic0;
-        if (it.n[1] > 0) ++ic1;
+        first = false;
       }
-      // every MMA this thread issued must finish before the TMEM is freed
-      mma_commit(&c.mma_final);
-      wait_phase_teardown(&c.mma_final, 0, 200000000ull);
-    }
-    __syncwarp();
+      // every copy this CTA started lands before its shared memory can go away (after an
+      // abort the consumers may never have waited for them)
+      for (int s = 0; s < NST; ++s)
+        if (issued & (1u << s)) wait_phase_teardown(&c.kv_full[s], (last_par >> s) & 1, 200000000ull);
+      for (int s = 0; s < NQ; ++s)
+        if (q_issued & (1u << s)) wait_phase_teardown(&c.q_full[s], (q_last >> s) & 1, 200000000ull);
+    } else if (warp == 1) {
+      // ------------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
+        uint32_t slot = 0, ring_par = 0, qs = 0, q_par = 0, fix_par = 0;
+        uint32_t pv0 = 0, pv1 = 0, pc0 = 0, pc1 = 0, ic0 = 0, ic1 = 0;  // per Q tile counters
+        bool ok = true;
+        for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+          const Item it = decode_item(idx, p, c);
+          if (it.nload == 0) continue;
+          uint32_t qslot[2];
+  #pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            qslot[t] = qs;
+            if (!wait_phase(&c.q_full[qs], q_par, wc)) ok = false;
+            if (++qs == NQ) { qs = 0; q_par ^= 1; }
+          }
+          if (!ok) break;
+          tc_fence_after();
+  #pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (it.n[t] == 0) mma_commit(&c.q_empty[qslot[t]]);  // never read: free at once
+          for (int j = 0; ok && j < it.nload; ++j) {
+            // S_t = Q_t K_j^T
+            if (!wait_phase(&c.kv_full[slot], ring_par, wc)) { ok = false; break; }
+            tc_fence_after();
+  #pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (j >= it.n[t]) continue;
+              const uint32_t pv = t == 0 ? pv0 : pv1;
+              // S_t's columns hold P_t(j-1) until that PV product completes
+              if (pv > 0 && !wait_phase(&c.o_done[t], (pv - 1) & 1, wc)) { ok = false; break; }
+              tc_fence_after();
+  #pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk / 4) * kQChunk + (kk % 4) * 32;
+                const uint64_t a = smem_desc_sw128(sQa + qslot[t] * kQTile + off, 16, 1024);
+                const uint64_t b = smem_desc_sw128(sKVa + slot * kKVTile + (kk / 4) * kKVChunk + (kk % 4) * 32, 16, 1024);
+                mma_ss(tmem + t * 128, a, b, kIdescS, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&c.s_full[t]);
+              if (j == it.n[t] - 1) mma_commit(&c.q_empty[qslot[t]]);  // last read of Q_t
+            }
+            if (!ok) break;
+            mma_commit(&c.kv_empty[slot]);
+            if (++slot == NST) { slot = 0; ring_par ^= 1; }
+            // O_t += P_t V_j
+            if (needs_fix(j, it.L, p.Skv)) {
+              if (!wait_phase(&c.kv_fixed[slot], (fix_par >> slot) & 1, wc)) { ok = false; break; }
+              fix_par ^= 1u << slot;
+            } else if (!wait_phase(&c.kv_full[slot], ring_par, wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int steps = pv_steps(j, it.L);
+  #pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (j >= it.n[t]) continue;
+              const uint32_t pc = t == 0 ? pc0 : pc1;
+              if (!wait_phase(&c.p_full[t], pc & 1, wc)) { ok = false; break; }
+              if (t == 0) ++pc0; else ++pc1;
+              const uint32_t ic = t == 0 ? ic0 : ic1;
+              if (j == 0 && !wait_phase(&c.o_free[t], (ic & 1) ^ 1, wc)) { ok = false; break; }
+              tc_fence_after();
+              for (int kk = 0; kk < steps; ++kk) {
+                const uint64_t b = smem_desc_sw128(sKVa + slot * kKVTile + kk * 16 * 128, kKVChunk, 1024);
+                mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, b, kIdescPV,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+              }
+              mma_commit(&c.o_done[t]);
+              if (t == 0) ++pv0; else ++pv1;
+            }
+            if (!ok) break;
+            mma_commit(&c.kv_empty[slot]);
+            if (++slot == NST) { slot = 0; ring_par ^= 1; }
+          }
+          if (!ok) break;
+          if (it.n[0] > 0) ++ic0;
+          if (it.n[1] > 0) ++ic1;
+        }
+        // every MMA this thread issued must finish before the TMEM is freed
+        mma_commit(&c.mma_final);
+        wait_phase_teardown(&c.mma_final, 0, 200000000ull);
+      }
+      __syncwarp();
+  }
   } else {
     // --------------------------------------------------------------------- softmax
-    const int t = (warp - 2) / 4;
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegsHigh) : "memory");
+    const int t = (warp - 4) / 4;
     const int quad = warp % 4;  // TMEM lanes a warp may touch: 32 * (warp % 4) ...
     const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -409,31 +421,23 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
         ++s_cnt;
         tc_fence_after();
         const int limit = kend - j * kBN;
-        // pass 1: the row max of the scaled scores over the visible
-        // keys, 8 independent chains; for a positive scale the max of the raw scores
+        // one TMEM round trip: the whole S row of this tile into registers
+        float s[kBN];
+        tmem_ld128(tS, reinterpret_cast<uint32_t*>(s));
+        // the row max of the scaled scores over the visible keys, 8 independent chains;
+        // for a positive scale the max of the raw scores, scaled once
         float mx8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx8[e] = -CUDART_INF_F;
+        const bool full = limit >= kBN;
+        if (pos_scale && full) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float s[64];
-          if (half == 0) {
-            tmem_ld64(tS, reinterpret_cast<uint32_t*>(s));
-          } else {
-            // half 0 is reduced to a single value before the second load is issued
-            mx8[0] = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            tmem_ld64_after(tS + 64, reinterpret_cast<uint32_t*>(s), mx8[0]);
-          }
-          if (pos_scale && limit >= kBN) {
+          for (int e = 0; e < kBN; ++e) mx8[e % 8] = fmaxf(mx8[e % 8], s[e]);
+        } else {
 #pragma unroll
-            for (int e = 0; e < 64; ++e) mx8[e % 8] = fmaxf(mx8[e % 8], s[e]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 64; ++e) {
-              const float v = pos_scale ? s[e] : s[e] * p.scale_log2;
-              mx8[e % 8] = fmaxf(mx8[e % 8], half * 64 + e < limit ? v : -CUDART_INF_F);
-            }
+          for (int e = 0; e < kBN; ++e) {
+            const float v = pos_scale ? s[e] : s[e] * p.scale_log2;
+            mx8[e % 8] = fmaxf(mx8[e % 8], e < limit ? v : -CUDART_INF_F);
           }
         }
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
@@ -457,28 +461,25 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
           }
         }
         if (raise) m = mnew;
-        // pass 2: P = 2^(s * scale * log2 e - m) in bf16, over the first half of S's
-        // columns; 32 columns per TMEM round trip keeps the register footprint small
+        // P = 2^(s * scale * log2 e - m) in bf16 over the first half of S's columns, a
+        // quarter at a time (the fence keeps each quarter after the previous store)
         const float msub = m == -CUDART_INF_F ? 0.f : m;
         float rs8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          float s[32];
-          if (q4 == 0) {
-            tmem_ld32(tS, reinterpret_cast<uint32_t*>(s));
-          } else {
-            rs8[0] = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-            rs8[1] = rs8[2] = rs8[3] = rs8[4] = rs8[5] = rs8[6] = rs8[7] = 0.f;
-            tmem_ld32_after(tS + q4 * 32, reinterpret_cast<uint32_t*>(s), rs8[0]);
-          }
           uint32_t pk[16];
+          if (q4 > 0) reg_fence32(s + q4 * 32);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int c0 = q4 * 32 + 2 * e;
-            const float x0 = c0 < limit ? fmaf(s[2 * e], p.scale_log2, -msub) : -CUDART_INF_F;
-            const float x1 = c0 + 1 < limit ? fmaf(s[2 * e + 1], p.scale_log2, -msub) : -CUDART_INF_F;
+            float x0 = fmaf(s[c0], p.scale_log2, -msub);
+            float x1 = fmaf(s[c0 + 1], p.scale_log2, -msub);
+            if (!full) {
+              x0 = c0 < limit ? x0 : -CUDART_INF_F;
+              x1 = c0 + 1 < limit ? x1 : -CUDART_INF_F;
+            }
             const float p0 = ex2_approx(x0);
             const float p1 = ex2_approx(x1);
             rs8[e % 8] += p0 + p1;
@@ -545,8 +546,15 @@ cudaError_t launch(const FwdParams& prm, int dev, cudaStream_t s) {
     std::lock_guard<std::mutex> lk(g_mu);
     const int which = D == 64 ? 0 : 1;
     if (!g_attr_set[dev][which]) {
-      cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D, NQ, NST>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      // the register split is only safe if the block launches with enough registers:
+      // a raise that the launch allocation cannot cover would wait forever
+      cudaFuncAttributes fa;
+      cudaError_t e = cudaFuncGetAttributes(&fa, fwd_sm103_kernel<D, NQ, NST>);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs * kThreads < 128 * kRegsLow + 256 * kRegsHigh || fa.numRegs > kLaunchRegs)
+        return cudaErrorInvalidConfiguration;
+      e = cudaFuncSetAttribute(fwd_sm103_kernel<D, NQ, NST>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
       g_attr_set[dev][which] = true;
     }

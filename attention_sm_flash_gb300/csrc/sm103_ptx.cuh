@@ -258,6 +258,19 @@ __device__ __forceinline__ void tmem_wait_st() {
 #undef ATTN_W4
 #undef ATTN_W16
 
+// An empty volatile statement that "rewrites" 32 registers: code that reads them cannot
+// be scheduled above it, and volatile statements keep their order, so it bounds how far
+// the compiler hoists work (and how many registers it keeps live).
+__device__ __forceinline__ void reg_fence32(float* v) {
+  asm volatile(""
+               : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
+                 "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
+                 "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]),
+                 "+f"(v[18]), "+f"(v[19]), "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]),
+                 "+f"(v[24]), "+f"(v[25]), "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]),
+                 "+f"(v[30]), "+f"(v[31]));
+}
+
 // ---------------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor of tcgen05: start address, leading-dimension byte
 // offset, stride-dimension byte offset (all >> 4), the fixed version field (bits 46-47
