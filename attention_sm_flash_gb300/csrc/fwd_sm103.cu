@@ -46,8 +46,8 @@ constexpr int kThreads = 384;    // warps 0-3: producer, MMA, 2 idle; 4-7, 8-11:
 // then drops to kRegsLow and the two softmax warpgroups rise to kRegsHigh. The raise
 // draws on the registers the block was launched with, so the split must fit in them.
 constexpr int kLaunchRegs = 168;
-constexpr int kRegsLow = 80;
-constexpr int kRegsHigh = 208;
+constexpr int kRegsLow = 112;
+constexpr int kRegsHigh = 192;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs, "register split");
 constexpr int kMaxSortedHeads = 64;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows > 2^8
@@ -303,9 +303,18 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
       // ------------------------------------------------------------------ MMA issuer
       if (lane == 0) {
         const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
-        uint32_t slot = 0, ring_par = 0, qs = 0, q_par = 0, fix_par = 0;
-        uint32_t pv0 = 0, pv1 = 0, pc0 = 0, pc1 = 0, ic0 = 0, ic1 = 0;  // per Q tile counters
+        // K-major Q and K tiles (128-byte rows, 8-row groups 1024 bytes apart); MN-major V
+        // (64-column chunks kKVChunk bytes apart)
+        const uint64_t desc_q0 = smem_desc_sw128(sQa, 16, 1024);
+        const uint64_t desc_k0 = smem_desc_sw128(sKVa, 16, 1024);
+        const uint64_t desc_v0 = smem_desc_sw128(sKVa, kKVChunk, 1024);
+        // K/V ring positions: tile j of an item uses 2 (kbase + j) (K) and 2 (kbase + j) + 1
+        // (V); a position's slot is pos % NST and its phase parity (pos / NST) & 1
+        uint32_t kbase = 0, qs = 0, q_par = 0, fix_par = 0;
+        uint32_t pv[2] = {0, 0}, pc[2] = {0, 0}, ic[2] = {0, 0};  // per Q tile counters
         bool ok = true;
+        auto slot_of = [](uint32_t pos) { return pos % NST; };
+        auto par_of = [](uint32_t pos) { return (pos / NST) & 1u; };
         for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
           const Item it = decode_item(idx, p, c);
           if (it.nload == 0) continue;
@@ -321,64 +330,99 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
   #pragma unroll
           for (int t = 0; t < 2; ++t)
             if (it.n[t] == 0) mma_commit(&c.q_empty[qslot[t]]);  // never read: free at once
-          for (int j = 0; ok && j < it.nload; ++j) {
-            // S_t = Q_t K_j^T
-            if (!wait_phase(&c.kv_full[slot], ring_par, wc)) { ok = false; break; }
+
+          // S_t(j) = Q_t K_j^T. S_t's columns hold P_t(j-1) until PV_t(j-1) completes.
+          auto issue_s = [&](int t, int j) -> bool {
+            if (pv[t] > 0 && !wait_phase(&c.o_done[t], (pv[t] - 1) & 1, wc)) return false;
             tc_fence_after();
+            const uint32_t kpos = 2 * (kbase + j);
+            const uint64_t a0 = desc_q0 + ((qslot[t] * kQTile) >> 4);
+            const uint64_t b0 = desc_k0 + ((slot_of(kpos) * kKVTile) >> 4);
   #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              if (j >= it.n[t]) continue;
-              const uint32_t pv = t == 0 ? pv0 : pv1;
-              // S_t's columns hold P_t(j-1) until that PV product completes
-              if (pv > 0 && !wait_phase(&c.o_done[t], (pv - 1) & 1, wc)) { ok = false; break; }
-              tc_fence_after();
-  #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk / 4) * kQChunk + (kk % 4) * 32;
-                const uint64_t a = smem_desc_sw128(sQa + qslot[t] * kQTile + off, 16, 1024);
-                const uint64_t b = smem_desc_sw128(sKVa + slot * kKVTile + (kk / 4) * kKVChunk + (kk % 4) * 32, 16, 1024);
-                mma_ss(tmem + t * 128, a, b, kIdescS, kk > 0 ? 1u : 0u);
-              }
-              mma_commit(&c.s_full[t]);
-              if (j == it.n[t] - 1) mma_commit(&c.q_empty[qslot[t]]);  // last read of Q_t
+            for (int kk = 0; kk < D / 16; ++kk) {
+              mma_ss(tmem + t * 128, a0 + (((kk / 4) * kQChunk + (kk % 4) * 32) >> 4),
+                     b0 + (((kk / 4) * kKVChunk + (kk % 4) * 32) >> 4), kIdescS, kk > 0 ? 1u : 0u);
             }
-            if (!ok) break;
-            mma_commit(&c.kv_empty[slot]);
-            if (++slot == NST) { slot = 0; ring_par ^= 1; }
-            // O_t += P_t V_j
+            mma_commit(&c.s_full[t]);
+            if (j == it.n[t] - 1) mma_commit(&c.q_empty[qslot[t]]);  // last read of Q_t
+            return true;
+          };
+          // O_t += P_t(j) V_j (the P_t(j) wait already done)
+          auto issue_pv = [&](int t, int j) -> bool {
+            if (j == 0 && !wait_phase(&c.o_free[t], (ic[t] & 1) ^ 1, wc)) return false;
+            tc_fence_after();
+            const int steps = pv_steps(j, it.L);
+            const uint64_t b0 = desc_v0 + ((slot_of(2 * (kbase + j) + 1) * kKVTile) >> 4);
+  #pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk) {
+              if (kk < steps)
+                mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, b0 + ((kk * 16 * 128) >> 4),
+                       kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&c.o_done[t]);
+            ++pv[t];
+            return true;
+          };
+          auto wait_k = [&](int j) -> bool {
+            const uint32_t kpos = 2 * (kbase + j);
+            if (!wait_phase(&c.kv_full[slot_of(kpos)], par_of(kpos), wc)) return false;
+            tc_fence_after();
+            return true;
+          };
+
+          // prologue: S_t(0) for both Q tiles
+          if (!wait_k(0)) { ok = false; break; }
+          for (int t = 0; t < 2 && ok; ++t)
+            if (it.n[t] > 0 && !issue_s(t, 0)) ok = false;
+          if (!ok) break;
+          mma_commit(&c.kv_empty[slot_of(2 * kbase)]);
+          // steady state, per Q tile: PV_t(j), then S_t(j + 1) once PV_t(j) has completed;
+          // Q tile 1's PV goes ahead of S_0(j + 1) when its P is already there
+          for (int j = 0; ok && j < it.nload; ++j) {
+            const uint32_t vpos = 2 * (kbase + j) + 1;
             if (needs_fix(j, it.L, p.Skv)) {
-              if (!wait_phase(&c.kv_fixed[slot], (fix_par >> slot) & 1, wc)) { ok = false; break; }
-              fix_par ^= 1u << slot;
-            } else if (!wait_phase(&c.kv_full[slot], ring_par, wc)) {
+              const uint32_t vs = slot_of(vpos);
+              if (!wait_phase(&c.kv_fixed[vs], (fix_par >> vs) & 1, wc)) { ok = false; break; }
+              fix_par ^= 1u << vs;
+            } else if (!wait_phase(&c.kv_full[slot_of(vpos)], par_of(vpos), wc)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const int steps = pv_steps(j, it.L);
-  #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              if (j >= it.n[t]) continue;
-              const uint32_t pc = t == 0 ? pc0 : pc1;
-              if (!wait_phase(&c.p_full[t], pc & 1, wc)) { ok = false; break; }
-              if (t == 0) ++pc0; else ++pc1;
-              const uint32_t ic = t == 0 ? ic0 : ic1;
-              if (j == 0 && !wait_phase(&c.o_free[t], (ic & 1) ^ 1, wc)) { ok = false; break; }
-              tc_fence_after();
-              for (int kk = 0; kk < steps; ++kk) {
-                const uint64_t b = smem_desc_sw128(sKVa + slot * kKVTile + kk * 16 * 128, kKVChunk, 1024);
-                mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, b, kIdescPV,
-                       (j > 0 || kk > 0) ? 1u : 0u);
+            bool pv1_done = j >= it.n[1];
+            bool k_next = false;
+            if (j < it.n[0]) {
+              if (!wait_phase(&c.p_full[0], pc[0] & 1, wc)) { ok = false; break; }
+              ++pc[0];
+              if (!issue_pv(0, j)) { ok = false; break; }
+              if (!pv1_done && mbar_test_wait(&c.p_full[1], pc[1] & 1)) {
+                ++pc[1];
+                if (!issue_pv(1, j)) { ok = false; break; }
+                pv1_done = true;
               }
-              mma_commit(&c.o_done[t]);
-              if (t == 0) ++pv0; else ++pv1;
+              if (j + 1 < it.n[0]) {
+                if (!wait_k(j + 1)) { ok = false; break; }
+                k_next = true;
+                if (!issue_s(0, j + 1)) { ok = false; break; }
+              }
             }
-            if (!ok) break;
-            mma_commit(&c.kv_empty[slot]);
-            if (++slot == NST) { slot = 0; ring_par ^= 1; }
+            if (!pv1_done) {
+              if (!wait_phase(&c.p_full[1], pc[1] & 1, wc)) { ok = false; break; }
+              ++pc[1];
+              if (!issue_pv(1, j)) { ok = false; break; }
+            }
+            if (j < it.n[1] && j + 1 < it.n[1]) {
+              if (!k_next && !wait_k(j + 1)) { ok = false; break; }
+              k_next = true;
+              if (!issue_s(1, j + 1)) { ok = false; break; }
+            }
+            mma_commit(&c.kv_empty[slot_of(vpos)]);
+            if (k_next) mma_commit(&c.kv_empty[slot_of(vpos + 1)]);
           }
           if (!ok) break;
-          if (it.n[0] > 0) ++ic0;
-          if (it.n[1] > 0) ++ic1;
+          kbase += it.nload;
+          if (it.n[0] > 0) ++ic[0];
+          if (it.n[1] > 0) ++ic[1];
         }
         // every MMA this thread issued must finish before the TMEM is freed
         mma_commit(&c.mma_final);
@@ -432,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
         const bool full = limit >= kBN;
         if (pos_scale && full) {
 #pragma unroll
-          for (int e = 0; e < kBN; ++e) mx8[e % 8] = fmaxf(mx8[e % 8], s[e]);
+          for (int e = 0; e < kBN / 2; ++e) mx8[e % 8] = max3f(mx8[e % 8], s[2 * e], s[2 * e + 1]);
         } else {
 #pragma unroll
           for (int e = 0; e < kBN; ++e) {
@@ -470,19 +514,19 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           uint32_t pk[16];
-          if (q4 > 0) reg_fence32(s + q4 * 32);
+          if (q4 > 0) reg_fence32(s + q4 * 32);  // after the previous quarter's store
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int c0 = q4 * 32 + 2 * e;
-            float x0 = fmaf(s[c0], p.scale_log2, -msub);
-            float x1 = fmaf(s[c0 + 1], p.scale_log2, -msub);
+            float x0, x1;
+            ffma2_bcast(x0, x1, s[c0], s[c0 + 1], p.scale_log2, -msub);
             if (!full) {
               x0 = c0 < limit ? x0 : -CUDART_INF_F;
               x1 = c0 + 1 < limit ? x1 : -CUDART_INF_F;
             }
             const float p0 = ex2_approx(x0);
             const float p1 = ex2_approx(x1);
-            rs8[e % 8] += p0 + p1;
+            fadd2_acc(rs8[2 * (e % 4)], rs8[2 * (e % 4) + 1], p0, p1);
             pk[e] = pack_bf16x2(p0, p1);
           }
           tmem_st16(tS + q4 * 16, pk);
