@@ -11,7 +11,8 @@
 // (batch, head), taken in a longest-first order:
 //   warp 0      TMA producer: a ring of Q tiles (the next item's Q is prefetched), and a
 //               ring of K/V tiles of 128 keys;
-//   warp 1      MMA issuer (one thread): S_t = Q_t K^T into TMEM, O_t += P_t V from TMEM;
+//   warps 1, 2  MMA issuers (one thread each, one per Q tile): S_t = Q_t K^T into TMEM,
+//               O_t += P_t V from TMEM;
 //   warps 4-7   softmax of Q tile 0 (128 rows, one row per thread);
 //   warps 8-11  softmax of Q tile 1.
 // TMEM (512 columns): S0 | S1 | O0 | O1. The softmax reads its S row, writes P (bf16)
@@ -41,7 +42,7 @@ using namespace sm103;
 constexpr int kBM = 128;         // rows of a Q tile (TMEM lanes)
 constexpr int kBN = 128;         // keys of a K/V tile
 constexpr int kItemRows = 2 * kBM;
-constexpr int kThreads = 384;    // warps 0-3: producer, MMA, 2 idle; 4-7, 8-11: softmax
+constexpr int kThreads = 384;    // warps 0-3: producer, 2 MMA issuers, idle; 4-7, 8-11: softmax
 // Register split (setmaxnreg): the block launches with kLaunchRegs a thread; warpgroup 0
 // then drops to kRegsLow and the two softmax warpgroups rise to kRegsHigh. The raise
 // draws on the registers the block was launched with, so the split must fit in them.
@@ -71,7 +72,7 @@ struct FwdParams {
 
 template <int NQ, int NST>
 struct FwdCtl {
-  uint64_t mma_final;
+  uint64_t mma_final[2];
   uint64_t q_full[NQ], q_empty[NQ];
   uint64_t kv_full[NST], kv_empty[NST], kv_fixed[NST];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
@@ -177,14 +178,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
 
   // ------------------------------------------------------------------- prologue
   if (threadIdx.x == 0) {
-    mbar_init(&c.mma_final, 1);
+    mbar_init(&c.mma_final[0], 1);
+    mbar_init(&c.mma_final[1], 1);
     for (int s = 0; s < NQ; ++s) {
       mbar_init(&c.q_full[s], 1);
       mbar_init(&c.q_empty[s], 1);
     }
     for (int s = 0; s < NST; ++s) {
       mbar_init(&c.kv_full[s], 1);
-      mbar_init(&c.kv_empty[s], 1);
+      mbar_init(&c.kv_empty[s], 2);  // released by both MMA issuers
       mbar_init(&c.kv_fixed[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
@@ -299,134 +301,85 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
         if (issued & (1u << s)) wait_phase_teardown(&c.kv_full[s], (last_par >> s) & 1, 200000000ull);
       for (int s = 0; s < NQ; ++s)
         if (q_issued & (1u << s)) wait_phase_teardown(&c.q_full[s], (q_last >> s) & 1, 200000000ull);
-    } else if (warp == 1) {
-      // ------------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 2) {
+      // ------------------------------------------------------------- MMA issuers
+      // one issuing thread per Q tile (warp 1: tile 0, warp 2: tile 1), so that each
+      // tile's S / PV chain advances as soon as its own softmax is done; both threads
+      // release every K/V slot (kv_empty counts two arrivals)
       if (lane == 0) {
+        const int t = warp - 1;
         const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
         // K-major Q and K tiles (128-byte rows, 8-row groups 1024 bytes apart); MN-major V
         // (64-column chunks kKVChunk bytes apart)
         const uint64_t desc_q0 = smem_desc_sw128(sQa, 16, 1024);
         const uint64_t desc_k0 = smem_desc_sw128(sKVa, 16, 1024);
         const uint64_t desc_v0 = smem_desc_sw128(sKVa, kKVChunk, 1024);
-        // K/V ring positions: tile j of an item uses 2 (kbase + j) (K) and 2 (kbase + j) + 1
-        // (V); a position's slot is pos % NST and its phase parity (pos / NST) & 1
-        uint32_t kbase = 0, qs = 0, q_par = 0, fix_par = 0;
-        uint32_t pv[2] = {0, 0}, pc[2] = {0, 0}, ic[2] = {0, 0};  // per Q tile counters
+        // ring positions: the k-th loaded item's Q tile t is Q position 2 k + t; its K/V
+        // tile j is at 2 (kbase + j) (K) and 2 (kbase + j) + 1 (V); a position's slot is
+        // pos % N and its phase parity (pos / N) % 2
+        uint32_t kbase = 0, qpos = t, fix_par = 0, pv = 0, pc = 0, ic = 0;
         bool ok = true;
-        auto slot_of = [](uint32_t pos) { return pos % NST; };
-        auto par_of = [](uint32_t pos) { return (pos / NST) & 1u; };
         for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
           const Item it = decode_item(idx, p, c);
           if (it.nload == 0) continue;
-          uint32_t qslot[2];
-  #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            qslot[t] = qs;
-            if (!wait_phase(&c.q_full[qs], q_par, wc)) ok = false;
-            if (++qs == NQ) { qs = 0; q_par ^= 1; }
-          }
-          if (!ok) break;
+          const int nt = t == 0 ? it.n[0] : it.n[1];
+          const uint32_t qslot = qpos % NQ;
+          if (!wait_phase(&c.q_full[qslot], (qpos / NQ) & 1, wc)) { ok = false; break; }
+          qpos += 2;
           tc_fence_after();
-  #pragma unroll
-          for (int t = 0; t < 2; ++t)
-            if (it.n[t] == 0) mma_commit(&c.q_empty[qslot[t]]);  // never read: free at once
-
-          // S_t(j) = Q_t K_j^T. S_t's columns hold P_t(j-1) until PV_t(j-1) completes.
-          auto issue_s = [&](int t, int j) -> bool {
-            if (pv[t] > 0 && !wait_phase(&c.o_done[t], (pv[t] - 1) & 1, wc)) return false;
-            tc_fence_after();
-            const uint32_t kpos = 2 * (kbase + j);
-            const uint64_t a0 = desc_q0 + ((qslot[t] * kQTile) >> 4);
-            const uint64_t b0 = desc_k0 + ((slot_of(kpos) * kKVTile) >> 4);
-  #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              mma_ss(tmem + t * 128, a0 + (((kk / 4) * kQChunk + (kk % 4) * 32) >> 4),
-                     b0 + (((kk / 4) * kKVChunk + (kk % 4) * 32) >> 4), kIdescS, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&c.s_full[t]);
-            if (j == it.n[t] - 1) mma_commit(&c.q_empty[qslot[t]]);  // last read of Q_t
-            return true;
-          };
-          // O_t += P_t(j) V_j (the P_t(j) wait already done)
-          auto issue_pv = [&](int t, int j) -> bool {
-            if (j == 0 && !wait_phase(&c.o_free[t], (ic[t] & 1) ^ 1, wc)) return false;
-            tc_fence_after();
-            const int steps = pv_steps(j, it.L);
-            const uint64_t b0 = desc_v0 + ((slot_of(2 * (kbase + j) + 1) * kKVTile) >> 4);
-  #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-              if (kk < steps)
-                mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, b0 + ((kk * 16 * 128) >> 4),
-                       kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(&c.o_done[t]);
-            ++pv[t];
-            return true;
-          };
-          auto wait_k = [&](int j) -> bool {
-            const uint32_t kpos = 2 * (kbase + j);
-            if (!wait_phase(&c.kv_full[slot_of(kpos)], par_of(kpos), wc)) return false;
-            tc_fence_after();
-            return true;
-          };
-
-          // prologue: S_t(0) for both Q tiles
-          if (!wait_k(0)) { ok = false; break; }
-          for (int t = 0; t < 2 && ok; ++t)
-            if (it.n[t] > 0 && !issue_s(t, 0)) ok = false;
-          if (!ok) break;
-          mma_commit(&c.kv_empty[slot_of(2 * kbase)]);
-          // steady state, per Q tile: PV_t(j), then S_t(j + 1) once PV_t(j) has completed;
-          // Q tile 1's PV goes ahead of S_0(j + 1) when its P is already there
+          if (nt == 0) mma_commit(&c.q_empty[qslot]);  // never read: free at once
           for (int j = 0; ok && j < it.nload; ++j) {
-            const uint32_t vpos = 2 * (kbase + j) + 1;
+            const uint32_t kpos = 2 * (kbase + j), vpos = kpos + 1;
+            const uint32_t ks = kpos % NST, vs = vpos % NST;
+            // S_t(j) = Q_t K_j^T; S_t's columns hold P_t(j - 1) until PV_t(j - 1) completes
+            if (!wait_phase(&c.kv_full[ks], (kpos / NST) & 1, wc)) { ok = false; break; }
+            if (j < nt) {
+              if (pv > 0 && !wait_phase(&c.o_done[t], (pv - 1) & 1, wc)) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t a0 = desc_q0 + ((qslot * kQTile) >> 4);
+              const uint64_t b0 = desc_k0 + ((ks * kKVTile) >> 4);
+  #pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                mma_ss(tmem + t * 128, a0 + (((kk / 4) * kQChunk + (kk % 4) * 32) >> 4),
+                       b0 + (((kk / 4) * kKVChunk + (kk % 4) * 32) >> 4), kIdescS, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&c.s_full[t]);
+              if (j == nt - 1) mma_commit(&c.q_empty[qslot]);  // last read of Q_t
+            }
+            mma_commit(&c.kv_empty[ks]);
+            // O_t += P_t(j) V_j
             if (needs_fix(j, it.L, p.Skv)) {
-              const uint32_t vs = slot_of(vpos);
               if (!wait_phase(&c.kv_fixed[vs], (fix_par >> vs) & 1, wc)) { ok = false; break; }
               fix_par ^= 1u << vs;
-            } else if (!wait_phase(&c.kv_full[slot_of(vpos)], par_of(vpos), wc)) {
+            } else if (!wait_phase(&c.kv_full[vs], (vpos / NST) & 1, wc)) {
               ok = false;
               break;
             }
-            tc_fence_after();
-            bool pv1_done = j >= it.n[1];
-            bool k_next = false;
-            if (j < it.n[0]) {
-              if (!wait_phase(&c.p_full[0], pc[0] & 1, wc)) { ok = false; break; }
-              ++pc[0];
-              if (!issue_pv(0, j)) { ok = false; break; }
-              if (!pv1_done && mbar_test_wait(&c.p_full[1], pc[1] & 1)) {
-                ++pc[1];
-                if (!issue_pv(1, j)) { ok = false; break; }
-                pv1_done = true;
+            if (j < nt) {
+              if (!wait_phase(&c.p_full[t], pc & 1, wc)) { ok = false; break; }
+              ++pc;
+              if (j == 0 && !wait_phase(&c.o_free[t], (ic & 1) ^ 1, wc)) { ok = false; break; }
+              tc_fence_after();
+              const int steps = pv_steps(j, it.L);
+              const uint64_t b0 = desc_v0 + ((vs * kKVTile) >> 4);
+  #pragma unroll
+              for (int kk = 0; kk < kBN / 16; ++kk) {
+                if (kk < steps)
+                  mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, b0 + ((kk * 16 * 128) >> 4),
+                         kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
               }
-              if (j + 1 < it.n[0]) {
-                if (!wait_k(j + 1)) { ok = false; break; }
-                k_next = true;
-                if (!issue_s(0, j + 1)) { ok = false; break; }
-              }
+              mma_commit(&c.o_done[t]);
+              ++pv;
             }
-            if (!pv1_done) {
-              if (!wait_phase(&c.p_full[1], pc[1] & 1, wc)) { ok = false; break; }
-              ++pc[1];
-              if (!issue_pv(1, j)) { ok = false; break; }
-            }
-            if (j < it.n[1] && j + 1 < it.n[1]) {
-              if (!k_next && !wait_k(j + 1)) { ok = false; break; }
-              k_next = true;
-              if (!issue_s(1, j + 1)) { ok = false; break; }
-            }
-            mma_commit(&c.kv_empty[slot_of(vpos)]);
-            if (k_next) mma_commit(&c.kv_empty[slot_of(vpos + 1)]);
+            mma_commit(&c.kv_empty[vs]);
           }
           if (!ok) break;
           kbase += it.nload;
-          if (it.n[0] > 0) ++ic[0];
-          if (it.n[1] > 0) ++ic[1];
+          if (nt > 0) ++ic;
         }
         // every MMA this thread issued must finish before the TMEM is freed
-        mma_commit(&c.mma_final);
-        wait_phase_teardown(&c.mma_final, 0, 200000000ull);
+        mma_commit(&c.mma_final[t]);
+        wait_phase_teardown(&c.mma_final[t], 0, 200000000ull);
       }
       __syncwarp();
   }
