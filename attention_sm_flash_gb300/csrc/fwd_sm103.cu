@@ -13,6 +13,7 @@
 //               ring of K/V tiles of 128 keys;
 //   warps 1, 2  MMA issuers (one thread each, one per Q tile): S_t = Q_t K^T into TMEM,
 //               O_t += P_t V from TMEM;
+//   warp 3      zeroes the padding rows of partial V tiles;
 //   warps 4-7   softmax of Q tile 0 (128 rows, one row per thread);
 //   warps 8-11  softmax of Q tile 1.
 // TMEM (512 columns): S0 | S1 | O0 | O1. The softmax reads its S row, writes P (bf16)
@@ -42,7 +43,7 @@ using namespace sm103;
 constexpr int kBM = 128;         // rows of a Q tile (TMEM lanes)
 constexpr int kBN = 128;         // keys of a K/V tile
 constexpr int kItemRows = 2 * kBM;
-constexpr int kThreads = 384;    // warps 0-3: producer, 2 MMA issuers, idle; 4-7, 8-11: softmax
+constexpr int kThreads = 384;    // warps 0-3: producer, 2 MMA issuers, V fixer; 4-7, 8-11: softmax
 // Register split (setmaxnreg): the block launches with kLaunchRegs a thread; warpgroup 0
 // then drops to kRegsLow and the two softmax warpgroups rise to kRegsHigh. The raise
 // draws on the registers the block was launched with, so the split must fit in them.
@@ -74,7 +75,7 @@ template <int NQ, int NST>
 struct FwdCtl {
   uint64_t mma_final[2];
   uint64_t q_full[NQ], q_empty[NQ];
-  uint64_t kv_full[NST], kv_empty[NST], kv_fixed[NST];
+  uint64_t kv_full[NST], kv_empty[NST], kv_fixed[NST], fix_req[NST];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
   uint32_t tmem_base;
   int abort;
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
       mbar_init(&c.kv_full[s], 1);
       mbar_init(&c.kv_empty[s], 2);  // released by both MMA issuers
       mbar_init(&c.kv_fixed[s], 1);
+      mbar_init(&c.fix_req[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&c.s_full[t], 1);
@@ -274,22 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
               issued |= 1u << slot;
               last_par = (last_par & ~(1u << slot)) | (ring_par << slot);
             }
-            if (kv == 1 && needs_fix(j, it.L, p.Skv)) {
-              // zero the padding rows of this V tile once it has landed
-              if (!wait_phase_warp(&c.kv_full[slot], ring_par, wc)) { ok = false; break; }
-              const int r0 = it.L - j * kBN;  // first padding row (>= 1: tile j holds valid keys)
-              const int units = (kBN - r0) * kChunks * 8;
-              uint8_t* base = sKV + slot * kKVTile;
-              for (int e = lane; e < units; e += 32) {
-                const int r = r0 + e / (kChunks * 8);
-                const int rest = e % (kChunks * 8);
-                *reinterpret_cast<uint4*>(base + (rest / 8) * kKVChunk + r * 128 + (rest % 8) * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-              }
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&c.kv_fixed[slot]);
-            }
+            // a V tile with padding rows: warp 3 zeroes them once the tile has landed
+            if (kv == 1 && needs_fix(j, it.L, p.Skv) && lane == 0) mbar_arrive(&c.fix_req[slot]);
             if (++slot == NST) { slot = 0; ring_par ^= 1; }
           }
         }
@@ -382,6 +370,37 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
         wait_phase_teardown(&c.mma_final[t], 0, 200000000ull);
       }
       __syncwarp();
+    } else {
+      // -------------------------------------------------------------- V-tile fixer
+      // zeroes the padding rows (at or past the valid length) of partial V tiles, so
+      // that 0 * NaN in the PV product cannot occur; requests come from the producer
+      // in ring order (fix_req), so the fill this waits for is never ambiguous
+      uint32_t kbase = 0, fr_par = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+        const Item it = decode_item(idx, p, c);
+        if (it.nload == 0) continue;
+        for (int j = 0; j < it.nload; ++j) {
+          if (!needs_fix(j, it.L, p.Skv)) continue;
+          const uint32_t vpos = 2 * (kbase + j) + 1, vs = vpos % NST;
+          if (!wait_phase_warp(&c.fix_req[vs], (fr_par >> vs) & 1, wc)) { ok = false; break; }
+          fr_par ^= 1u << vs;
+          if (!wait_phase_warp(&c.kv_full[vs], (vpos / NST) & 1, wc)) { ok = false; break; }
+          const int r0 = it.L - j * kBN;  // first padding row (>= 1: tile j holds valid keys)
+          const int units = (kBN - r0) * kChunks * 8;
+          uint8_t* base = sKV + vs * kKVTile;
+          for (int e = lane; e < units; e += 32) {
+            const int r = r0 + e / (kChunks * 8);
+            const int rest = e % (kChunks * 8);
+            *reinterpret_cast<uint4*>(base + (rest / 8) * kKVChunk + r * 128 + (rest % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&c.kv_fixed[vs]);
+        }
+        kbase += it.nload;
+      }
   }
   } else {
     // --------------------------------------------------------------------- softmax
