@@ -64,6 +64,7 @@ struct FwdParams {
   unsigned int* err;
   int B, Hq, Hkv, Sq, Skv;
   int causal;
+  int head_inner;    // non-causal order with the (batch, head) index innermost
   int n_qblocks;
   int n_items;
   float scale_log2;  // scale * log2(e)
@@ -111,7 +112,16 @@ __device__ __forceinline__ Item decode_item(int idx, const FwdParams& p, const C
     b = bk / p.Hkv;
     h = (bk % p.Hkv) * g + rem / p.n_qblocks;
     qb = rem % p.n_qblocks;
+  } else if (p.head_inner) {
+    // short K/V (L2-resident): concurrent CTAs cover every head of the same query rows,
+    // so Q is read and O written as whole contiguous rows across heads
+    const int BH = p.B * p.Hq;
+    qb = idx / BH;
+    const int bh = idx % BH;
+    b = bh / p.Hq;
+    h = bh % p.Hq;
   } else {
+    // long K/V: consecutive query blocks of one head run together and share K/V in L2
     const int bh = idx / p.n_qblocks;
     qb = idx % p.n_qblocks;
     b = bh / p.Hq;
@@ -657,6 +667,8 @@ cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
   prm.Sq = p.Sq;
   prm.Skv = p.Skv;
   prm.causal = p.causal;
+  // K/V of every head small enough to stay in L2 (a third of its 129 MB)
+  prm.head_inner = (double)p.B * p.Hkv * p.Skv * p.D * 2 * 2 <= 43.0e6 ? 1 : 0;
   prm.n_qblocks = (p.Sq + kItemRows - 1) / kItemRows;
   prm.n_items = p.B * p.Hq * prm.n_qblocks;
   prm.scale_log2 = p.scale * 1.4426950408889634f;
