@@ -61,7 +61,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp,
                              i, vp, sz, vp]
     lib.attn_bwd_workspace_size.restype = sz
-    lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
+    lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
     lib.attn_peek_device_error.restype = i
     lib.attn_peek_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
     lib.attn_status_string.restype = ctypes.c_char_p
@@ -147,8 +147,9 @@ def attn_fwd(q, k, v, o, lse, causal: bool = False, scale: float | None = None,
         raise AttnError(st, "attn_fwd")
 
 
-def attn_bwd_workspace_size(B: int, Hq: int, Sq: int, D: int, dtype_code: int) -> int:
-    return int(load().attn_bwd_workspace_size(B, Hq, Sq, D, dtype_code))
+def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,
+                            dtype_code: int) -> int:
+    return int(load().attn_bwd_workspace_size(B, Hq, Hkv, Sq, Skv, D, dtype_code))
 
 
 def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal: bool = False,
@@ -161,7 +162,7 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal: bool = False,
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     code = _dtype_code(q)
-    need = attn_bwd_workspace_size(B, Hq, Sq, D, code)
+    need = attn_bwd_workspace_size(B, Hq, Hkv, Sq, Skv, D, code)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     st = load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),

@@ -97,12 +97,13 @@ extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, v
   return from_cuda(dtype == ATTN_BF16 ? tc_fwd(p, s) : simt_fwd(p, s));
 }
 
-extern "C" size_t attn_bwd_workspace_size(int B, int Hq, int Sq, int D, attn_dtype_t dtype) {
-  (void)D;
-  (void)dtype;
-  if (B <= 0 || Hq <= 0 || Sq <= 0) return 0;
-  const size_t delta = (size_t)B * Hq * Sq * sizeof(float);
-  return (delta + 255) / 256 * 256;
+extern "C" size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                                          attn_dtype_t dtype) {
+  if (B <= 0 || Hq <= 0 || Sq <= 0 || Hkv <= 0 || Skv < 0 || D <= 0) return 0;
+  size_t n = bwd_delta_bytes(B, Hq, Sq);
+  if (Skv > 0 && Hq % Hkv == 0 && bwd_split_heads(B, Hq, Hkv, Skv, dtype))
+    n += 2 * bwd_partial_bytes(B, Hq, Skv, D);
+  return n;
 }
 
 extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -132,12 +133,18 @@ extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, c
       !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
       !aligned(lse, 4))
     return ATTN_ERR_INVALID_ARG;
-  const size_t need = attn_bwd_workspace_size(B, Hq, Sq, D, dtype);
+  const size_t need = attn_bwd_workspace_size(B, Hq, Hkv, Sq, Skv, D, dtype);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
     return ATTN_ERR_WORKSPACE;
   Problem p{};
   p.q = q; p.k = k; p.v = v; p.o_in = o; p.dout = dout; p.lse = const_cast<float*>(lse);
   p.dq = dq; p.dk = dk; p.dv = dv; p.delta = static_cast<float*>(workspace);
+  p.split = Skv > 0 && bwd_split_heads(B, Hq, Hkv, Skv, dtype) ? 1 : 0;
+  if (p.split) {
+    uint8_t* w = static_cast<uint8_t*>(workspace) + bwd_delta_bytes(B, Hq, Sq);
+    p.part_dk = reinterpret_cast<float*>(w);
+    p.part_dv = reinterpret_cast<float*>(w + bwd_partial_bytes(B, Hq, Skv, D));
+  }
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.D = D;
   p.scale = scale; p.causal = causal; p.kv_lens = kv_lens; p.dtype = dtype;
   cudaError_t e = error_word(&p.err);

@@ -22,6 +22,9 @@ struct Problem {
   void* dk;
   void* dv;
   float* delta;       // backward workspace: rowsum(dO * O), [B, Hq, Sq]
+  float* part_dk;     // backward workspace when the GQA group is split: fp32 [B, Skv, Hq, D]
+  float* part_dv;
+  int split;          // 1: dK/dV per (key tile, query head) + an ordered group reduction
   int B, Hq, Hkv, Sq, Skv, D;
   float scale;
   int causal;
@@ -29,6 +32,20 @@ struct Problem {
   attn_dtype_t dtype;
   unsigned int* err;       // device error word (ATTN_DEVERR_* bits)
 };
+
+// Whether the bf16 backward splits each GQA group into one dK/dV work item per query
+// head (fp32 partial dK/dV in the workspace, then a reduction over the group in a
+// fixed order): done when (batch, kv head, 128-key tile) items alone are too few to
+// balance the GPU. A pure function of the sizes, so that the workspace query and the
+// launch agree.
+inline bool bwd_split_heads(int B, int Hq, int Hkv, int Skv, attn_dtype_t dtype) {
+  return dtype == ATTN_BF16 && Hq > Hkv && (long long)B * Hkv * ((Skv + 127) / 128) < 256;
+}
+inline size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+inline size_t bwd_delta_bytes(int B, int Hq, int Sq) { return round256((size_t)B * Hq * Sq * sizeof(float)); }
+inline size_t bwd_partial_bytes(int B, int Hq, int Skv, int D) {
+  return round256((size_t)B * Skv * Hq * D * sizeof(float));
+}
 
 // Counts one kernel launch issued by the library (see attn_launch_count()).
 void count_launches(int n);

@@ -45,7 +45,7 @@ extern "C" attn_status_t attn_bwd_noalloc(const void* q, const void* k, const vo
                                           int Hkv, int Sq, int Skv, int D, float scale,
                                           int causal, const int32_t* kv_lens,
                                           attn_dtype_t dtype, attn_stream_t stream) {
-  const size_t need = attn_bwd_workspace_size(B, Hq, Sq, D, dtype);
+  const size_t need = attn_bwd_workspace_size(B, Hq, Hkv, Sq, Skv, D, dtype);
   if (need > (size_t)ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (need > 0 && scratch_address(&scratch) != cudaSuccess) return ATTN_ERR_CUDA;

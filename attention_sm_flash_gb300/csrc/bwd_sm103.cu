@@ -9,7 +9,10 @@
 //
 // dK/dV: a CTA owns 128 keys of one (batch, kv head) and loops over the query heads of
 //   the GQA group and their query tiles of 64 rows in a fixed order, so the group sum of
-//   row T15 (in-group deterministic sum) happens inside its TMEM accumulators. Keys sit
+//   row T15 (in-group deterministic sum) happens inside its TMEM accumulators. When such
+//   items are too few to fill the GPU (few kv heads, causal imbalance), each query head
+//   is its own item writing fp32 partial dK/dV, and a reduction kernel sums each group
+//   in head order - still deterministic, still no atomics. Keys sit
 //   on the TMEM lanes: S^T = K Q^T and dP^T = V dO^T (M = 128 keys, N = 64 queries), the
 //   elementwise warps turn them into P^T and dS^T (bf16, written back over the first
 //   half of the same columns), then dV += P^T dO and dK += dS^T Q with A from TMEM.
@@ -50,9 +53,12 @@ struct BwdParams {
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
+  float* part_dk;  // split mode: fp32 per-query-head partial dK, dV [B, Skv, Hq, D]
+  float* part_dv;
   const int32_t* kv_lens;
   unsigned int* err;
   int B, Hq, Hkv, Sq, Skv, causal;
+  int split;
   int n_items;
   float scale, scale_log2;
   uint64_t timeout_ns;
@@ -95,22 +101,29 @@ struct DkvCtl {
 
 struct DkvItem {
   int b, kvh, j0, L;
+  int h0, heads;  // query heads h0 .. h0 + heads - 1 (the whole group, or one in split mode)
   int i_start, per_head, n_tiles;
 };
 
 __device__ __forceinline__ DkvItem dkv_decode(int idx, const BwdParams& p) {
   const int n_kt = (p.Skv + kKeys - 1) / kKeys;
+  const int g = p.Hq / p.Hkv;
+  const int gs = p.split ? g : 1;  // items per (batch, kv head, key tile)
   const int BK = p.B * p.Hkv;
-  int b, kvh, kt;
+  int b, kvh, kt, r;
   if (p.causal) {
     // longest first: the first key tiles are seen by the most queries
-    kt = idx / BK;
-    const int bk = idx % BK;
+    kt = idx / (BK * gs);
+    const int rem = idx % (BK * gs);
+    const int bk = rem / gs;
+    r = rem % gs;
     b = bk / p.Hkv;
     kvh = bk % p.Hkv;
   } else {
-    const int bk = idx / n_kt;
-    kt = idx % n_kt;
+    const int bk = idx / (n_kt * gs);
+    const int rem = idx % (n_kt * gs);
+    kt = rem / gs;
+    r = rem % gs;
     b = bk / p.Hkv;
     kvh = bk % p.Hkv;
   }
@@ -119,6 +132,8 @@ __device__ __forceinline__ DkvItem dkv_decode(int idx, const BwdParams& p) {
   it.kvh = kvh;
   it.j0 = kt * kKeys;
   it.L = kv_len_of(p, b, kvh);
+  it.h0 = kvh * g + r;
+  it.heads = p.split ? 1 : g;
   const int n_qt = (p.Sq + kQT - 1) / kQT;
   it.i_start = 0;
   it.per_head = 0;
@@ -128,7 +143,7 @@ __device__ __forceinline__ DkvItem dkv_decode(int idx, const BwdParams& p) {
     it.i_start = first / kQT;
     it.per_head = max(0, n_qt - it.i_start);
   }
-  it.n_tiles = (p.Hq / p.Hkv) * it.per_head;
+  it.n_tiles = it.heads * it.per_head;
   return it;
 }
 
@@ -206,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
       }
       ++kv_cnt;
       for (int t = 0; t < it.n_tiles; ++t) {
-        const int h = it.kvh * g + t / it.per_head;
+        const int h = it.h0 + t / it.per_head;
         const int i0 = (it.i_start + t % it.per_head) * kQT;
         if (!wait_phase_warp(&c.st_empty[st], st_par ^ 1, wc)) { ok = false; break; }
         if (lane == 0) {
@@ -325,7 +340,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
       const bool key_ok = j < it.L;
       const int64_t orow = ((static_cast<int64_t>(it.b) * p.Skv + j) * p.Hkv + it.kvh) * D;
       if (it.n_tiles == 0) {
-        if (j < p.Skv) zero_row_bf16((w == 0 ? p.dv : p.dk) + orow, D);
+        if (j < p.Skv) {
+          if (p.split) {
+            float4* z = reinterpret_cast<float4*>((w == 0 ? p.part_dv : p.part_dk) +
+                                                  ((static_cast<int64_t>(it.b) * p.Skv + j) * p.Hq + it.h0) * D);
+            for (int d = 0; d < D / 4; ++d) z[d] = make_float4(0.f, 0.f, 0.f, 0.f);
+          } else {
+            zero_row_bf16((w == 0 ? p.dv : p.dk) + orow, D);
+          }
+        }
         continue;
       }
       for (int t = 0; t < it.n_tiles; ++t, ++gt) {
@@ -372,6 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
       if (!wait_phase_warp(&c.acc_done, item_cnt & 1, wc)) { ok = false; break; }
       tc_fence_after();
       __nv_bfloat16* dst = (w == 0 ? p.dv : p.dk) + orow;
+      float* pdst = (w == 0 ? p.part_dv : p.part_dk) +
+                    ((static_cast<int64_t>(it.b) * p.Skv + j) * p.Hq + it.h0) * D;
       const uint32_t tacc = tmem + lane_off + (w == 0 ? 0 : D);
       const float mul = w == 0 ? 1.f : p.scale;
 #pragma unroll
@@ -379,8 +404,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         uint32_t v[32];
         tmem_ld32(tacc + cc * 32, v);
         if (j < p.Skv) {
-          if (key_ok) store_row_bf16(dst + cc * 32, v, mul);
-          else zero_row_bf16(dst + cc * 32, 32);
+          if (p.split) {
+            // this query head's share, unscaled; the group reduction scales dK
+            float4* d4 = reinterpret_cast<float4*>(pdst + cc * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              d4[e] = key_ok ? make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                           __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+          } else if (key_ok) {
+            store_row_bf16(dst + cc * 32, v, mul);
+          } else {
+            zero_row_bf16(dst + cc * 32, 32);
+          }
         }
       }
       tc_fence_before();
@@ -698,6 +734,37 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_sm103_kernel(const __grid_
   }
 }
 
+// ===================================================================== group reduction
+// Split mode: dK[b, j, kvh] = scale * sum over the group's query heads r = 0 .. g - 1 (in
+// that order) of the partial dK[b, j, kvh * g + r]; likewise dV (unscaled). Each thread
+// reduces 4 consecutive elements of one (b, j, kvh) row.
+__global__ void __launch_bounds__(256) bwd_group_reduce_kernel(const float* __restrict__ part_dk,
+                                                               const float* __restrict__ part_dv,
+                                                               __nv_bfloat16* dk, __nv_bfloat16* dv,
+                                                               int B, int Skv, int Hq, int Hkv, int D,
+                                                               float scale) {
+  const int g = Hq / Hkv;
+  const int64_t n4 = (int64_t)B * Skv * Hkv * D / 4;
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= n4) return;
+  const int d4 = (int)(e % (D / 4));
+  const int64_t row = e / (D / 4);  // (b * Skv + j) * Hkv + kvh
+  const int kvh = (int)(row % Hkv);
+  const int64_t bj = row / Hkv;
+  const int64_t src0 = (bj * Hq + (int64_t)kvh * g) * D + 4 * d4;
+  float4 sk = make_float4(0.f, 0.f, 0.f, 0.f), sv = sk;
+  for (int r = 0; r < g; ++r) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(part_dk + src0 + (int64_t)r * D));
+    const float4 c = __ldg(reinterpret_cast<const float4*>(part_dv + src0 + (int64_t)r * D));
+    sk.x += a.x; sk.y += a.y; sk.z += a.z; sk.w += a.w;
+    sv.x += c.x; sv.y += c.y; sv.z += c.z; sv.w += c.w;
+  }
+  const int64_t dst = row * D + 4 * d4;
+  *reinterpret_cast<uint2*>(dk + dst) =
+      make_uint2(pack_bf16x2(sk.x * scale, sk.y * scale), pack_bf16x2(sk.z * scale, sk.w * scale));
+  *reinterpret_cast<uint2*>(dv + dst) = make_uint2(pack_bf16x2(sv.x, sv.y), pack_bf16x2(sv.z, sv.w));
+}
+
 // ============================================================================ host side
 template <int D, int NST>
 constexpr size_t dkdv_smem() {
@@ -742,6 +809,9 @@ cudaError_t launch_bwd(const Problem& p, int dev, cudaStream_t s) {
   prm.dq = static_cast<__nv_bfloat16*>(p.dq);
   prm.dk = static_cast<__nv_bfloat16*>(p.dk);
   prm.dv = static_cast<__nv_bfloat16*>(p.dv);
+  prm.part_dk = p.part_dk;
+  prm.part_dv = p.part_dv;
+  prm.split = p.split;
   prm.kv_lens = p.kv_lens;
   prm.err = p.err;
   prm.B = p.B;
@@ -755,7 +825,7 @@ cudaError_t launch_bwd(const Problem& p, int dev, cudaStream_t s) {
   prm.timeout_ns = 4000000000ull;
   const int sms = g_num_sms[dev];
   if (p.Skv > 0) {
-    prm.n_items = p.B * p.Hkv * ((p.Skv + kKeys - 1) / kKeys);
+    prm.n_items = p.B * p.Hkv * ((p.Skv + kKeys - 1) / kKeys) * (p.split ? p.Hq / p.Hkv : 1);
     constexpr size_t smem = dkdv_smem<D, NST_KV>();
     cudaError_t e = set_smem(bwd_dkdv_sm103_kernel<D, NST_KV>, smem, dev, D == 64 ? 0 : 1);
     if (e != cudaSuccess) return e;
@@ -763,6 +833,14 @@ cudaError_t launch_bwd(const Problem& p, int dev, cudaStream_t s) {
     count_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (p.split) {
+      const int64_t n4 = (int64_t)p.B * p.Skv * p.Hkv * D / 4;
+      bwd_group_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
+          p.part_dk, p.part_dv, prm.dk, prm.dv, p.B, p.Skv, p.Hq, p.Hkv, D, p.scale);
+      count_launches(1);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
   }
   // the dQ kernel tiles K/V by 64 keys and Q/dO by 128 rows
   if (!make_bshd_map(&prm.tm_q, p.q, p.B, p.Sq, p.Hq, D, kQRows) ||

@@ -276,7 +276,7 @@ def run_ours(args, rank, world, local_rank):
     lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
     if w.has_bwd:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        ws_bytes = attn.attn_bwd_workspace_size(w.B, w.Hq, w.Sq, w.D,
+        ws_bytes = attn.attn_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D,
                                                 attn.ATTN_BF16 if w.dtype == "bf16" else attn.ATTN_F32)
         ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.int16, device=dev)  # 512 MiB

@@ -100,7 +100,8 @@ ATTN_API attn_status_t attn_fwd(const void* q, const void* k, const void* v, voi
  * dv must be 16-byte aligned and `workspace` must hold at least
  * attn_bwd_workspace_size(...) bytes of device memory, 256-byte aligned, for the call's
  * exclusive use until the stream reaches the end of the call (ATTN_ERR_WORKSPACE
- * otherwise). The workspace holds delta = rowsum(dO * O) [B, Hq, Sq] fp32.
+ * otherwise). The workspace holds delta = rowsum(dO * O) [B, Hq, Sq] fp32 and, when
+ * attn_bwd_workspace_size() says so, fp32 partial dK/dV of each query head.
  */
 ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
@@ -108,8 +109,12 @@ ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, con
                        int causal, const int32_t* kv_lens, attn_dtype_t dtype,
                        void* workspace, size_t workspace_bytes, attn_stream_t stream);
 
-/* Bytes of device workspace attn_bwd needs for these sizes (0 for an empty problem). */
-ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Sq, int D, attn_dtype_t dtype);
+/* Bytes of device workspace attn_bwd needs for these sizes (0 for an empty problem):
+ * delta [B, Hq, Sq] fp32, plus, for bf16 GQA problems with few (batch, kv head, key
+ * tile) work items, fp32 per-query-head partial dK and dV [B, Skv, Hq, D] that a
+ * second kernel sums over each group in a fixed order. A pure function of the sizes. */
+ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                                        attn_dtype_t dtype);
 
 /* Size of the library's static device scratch array used by attn_bwd_noalloc: 8 MiB,
  * enough for B * Hq * Sq <= 2,097,152 query rows. */

@@ -39,9 +39,16 @@ def test_status_strings_and_build_info(lib):
 
 
 def test_workspace_size(lib):
-    n = attn.attn_bwd_workspace_size(4, 8, 2048, 128, attn.ATTN_BF16)
-    assert n >= 4 * 8 * 2048 * 4 and n % 256 == 0
-    assert attn.attn_bwd_workspace_size(0, 8, 2048, 128, attn.ATTN_BF16) == 0
+    # MHA: delta only
+    n = attn.attn_bwd_workspace_size(8, 12, 12, 1024, 1024, 64, attn.ATTN_BF16)
+    assert n == 8 * 12 * 1024 * 4
+    # GQA with few (batch, kv head, key tile) items: delta + fp32 partial dK, dV per head
+    n = attn.attn_bwd_workspace_size(4, 8, 2, 2048, 2048, 128, attn.ATTN_BF16)
+    assert n == 4 * 8 * 2048 * 4 + 2 * 4 * 2048 * 8 * 128 * 4 and n % 256 == 0
+    # many items, or fp32: delta only
+    assert attn.attn_bwd_workspace_size(64, 8, 2, 2048, 2048, 128, attn.ATTN_BF16) == 64 * 8 * 2048 * 4
+    assert attn.attn_bwd_workspace_size(4, 8, 2, 2048, 2048, 128, attn.ATTN_F32) == 4 * 8 * 2048 * 4
+    assert attn.attn_bwd_workspace_size(0, 8, 2, 2048, 2048, 128, attn.ATTN_BF16) == 0
 
 
 A = 0x10000  # a fake, 256-byte aligned "device address": never dereferenced here
