@@ -53,7 +53,8 @@ void count_launches(int n);
 // CUDA-core kernels (fp32 arithmetic): the fp32 path, any D in {64, 128}.
 cudaError_t simt_fwd(const Problem& p, cudaStream_t stream);
 cudaError_t simt_bwd(const Problem& p, cudaStream_t stream);
-// delta = rowsum(dO * O) into p.delta (one warp per row); used by both backward paths.
+// delta = rowsum(dO * O) into p.delta (one warp per row), for the CUDA-core backward
+// (the bf16 backward forms delta inside its dQ kernel).
 cudaError_t simt_delta(const Problem& p, cudaStream_t stream);
 
 // Tensor-core (tcgen05) kernels for bf16, sm_103a.
