@@ -22,9 +22,11 @@
 //   in head order - still deterministic, still no atomics. Keys sit on the TMEM lanes:
 //   S^T = K Q^T and dP^T = V dO^T; the elementwise warps write P^T and dS^T (bf16) over
 //   the first columns of each, and dV += P^T dO, dK += dS^T Q take A from TMEM. The MMAs
-//   of one tile are issued S^T, dP^T, dV, dK, so that each wait of the issuing thread
+//   of one tile are issued S^T, dP^T, dV, dK, so that each wait of the issuing threads
 //   (P^T ready, dS^T ready, S^T's columns free, dP^T's columns free) sits behind an MMA
-//   already queued and the tensor pipe does not drain between tiles.
+//   already queued. (Double-buffering 64-query S^T / dP^T tiles instead measured slower:
+//   N = 64 MMAs are shared-memory bound and the tensor pipe then runs mixed SS / TS work
+//   from two issuing threads.)
 //
 // Roles (384 threads): warp 0 TMA producer; two MMA-issuing threads, one in warp 1 for the
 // products that recompute S and dP, one in warp 10 for the accumulations (dQ, or dV and
@@ -109,13 +111,13 @@ __device__ __forceinline__ int item_at(int pass) {
   return (pass & 1) ? (pass + 1) * G - 1 - c : pass * G + c;
 }
 
-// Loads that the SW128 K-major / MN-major descriptors below address: a tile of kT rows
-// and D columns is D / 64 chunks of kT rows x 128 bytes (8-row groups 1024 bytes apart).
+// Loads that the SW128 K-major / MN-major descriptors below address: a tile of `rows`
+// rows and D columns is D / 64 chunks of rows x 128 bytes (8-row groups 1024 bytes apart).
 template <int D>
 __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int head,
-                                          int row0, int b) {
+                                          int row0, int b, int rows) {
 #pragma unroll
-  for (int ch = 0; ch < D / 64; ++ch) tma_load_4d(dst + ch * kT * 128, map, bar, ch * 64, head, row0, b);
+  for (int ch = 0; ch < D / 64; ++ch) tma_load_4d(dst + ch * rows * 128, map, bar, ch * 64, head, row0, b);
 }
 
 // =============================================================================== dQ
@@ -254,13 +256,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_sm103_kernel(const __grid_
       if (!wait_phase_warp(&c.q_empty, (q_cnt & 1) ^ 1, wc)) { ok = false; break; }
       if (lane == 0) {
         mbar_expect_tx(&c.q_full, kTile);
-        load_tile<D>(sQ, &p.tm_q, &c.q_full, it.h, it.q0, it.b);
+        load_tile<D>(sQ, &p.tm_q, &c.q_full, it.h, it.q0, it.b, kT);
       }
       ++q_cnt;
       if (!wait_phase_warp(&c.do_empty, (do_cnt & 1) ^ 1, wc)) { ok = false; break; }
       if (lane == 0) {
         mbar_expect_tx(&c.do_full, kTile);
-        load_tile<D>(sdO, &p.tm_do, &c.do_full, it.h, it.q0, it.b);
+        load_tile<D>(sdO, &p.tm_do, &c.do_full, it.h, it.q0, it.b, kT);
       }
       ++do_cnt;
       for (int jt = 0; jt < it.n_tiles; ++jt, ++kpos, ++vpos) {
@@ -269,14 +271,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_sm103_kernel(const __grid_
         if (!wait_phase_warp(&c.k_empty[ks], kpar ^ 1, wc)) { ok = false; break; }
         if (lane == 0) {
           mbar_expect_tx(&c.k_full[ks], kTile);
-          load_tile<D>(sK + ks * kTile, &p.tm_k, &c.k_full[ks], it.kvh, jt * kT, it.b);
+          load_tile<D>(sK + ks * kTile, &p.tm_k, &c.k_full[ks], it.kvh, jt * kT, it.b, kT);
         }
         k_iss |= 1u << ks;
         k_last = (k_last & ~(1u << ks)) | (kpar << ks);
         if (!wait_phase_warp(&c.v_empty[vs], vpar ^ 1, wc)) { ok = false; break; }
         if (lane == 0) {
           mbar_expect_tx(&c.v_full[vs], kTile);
-          load_tile<D>(sV + vs * kTile, &p.tm_v, &c.v_full[vs], it.kvh, jt * kT, it.b);
+          load_tile<D>(sV + vs * kTile, &p.tm_v, &c.v_full[vs], it.kvh, jt * kT, it.b, kT);
         }
         v_iss |= 1u << vs;
         v_last = (v_last & ~(1u << vs)) | (vpar << vs);
@@ -649,13 +651,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
       if (!wait_phase_warp(&c.k_empty, (k_cnt & 1) ^ 1, wc)) { ok = false; break; }
       if (lane == 0) {
         mbar_expect_tx(&c.k_full, kTile);
-        load_tile<D>(sK, &p.tm_k, &c.k_full, it.kvh, it.j0, it.b);
+        load_tile<D>(sK, &p.tm_k, &c.k_full, it.kvh, it.j0, it.b, kT);
       }
       ++k_cnt;
       if (!wait_phase_warp(&c.v_empty, (v_cnt & 1) ^ 1, wc)) { ok = false; break; }
       if (lane == 0) {
         mbar_expect_tx(&c.v_full, kTile);
-        load_tile<D>(sV, &p.tm_v, &c.v_full, it.kvh, it.j0, it.b);
+        load_tile<D>(sV, &p.tm_v, &c.v_full, it.kvh, it.j0, it.b, kT);
       }
       ++v_cnt;
       for (int t = 0; t < it.n_tiles; ++t) {
@@ -664,8 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         if (!wait_phase_warp(&c.st_empty[st], st_par ^ 1, wc)) { ok = false; break; }
         if (lane == 0) {
           mbar_expect_tx(&c.st_full[st], 2 * kTile);
-          load_tile<D>(sQ + st * kTile, &p.tm_q, &c.st_full[st], h, i0, it.b);
-          load_tile<D>(sdO + st * kTile, &p.tm_do, &c.st_full[st], h, i0, it.b);
+          load_tile<D>(sQ + st * kTile, &p.tm_q, &c.st_full[st], h, i0, it.b, kT);
+          load_tile<D>(sdO + st * kTile, &p.tm_do, &c.st_full[st], h, i0, it.b, kT);
         }
         issued |= 1u << st;
         last_par = (last_par & ~(1u << st)) | (st_par << st);
@@ -810,13 +812,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
       for (int t = 0; t < it.n_tiles; ++t, ++gt) {
         const uint32_t s = gt % NST;
         if (!wait_phase_warp(&c.st_full[s], (gt / NST) & 1, wc)) { ok = false; break; }
+        // the tile's per-column -LSE go to registers before the wait for S^T: while SS MMAs
+        // run they take the whole shared-memory bandwidth, and a load issued on the
+        // critical path costs several hundred cycles
+        float4 nlv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) nlv[e] = reinterpret_cast<const float4*>(&c.nlse[s][64 * hsel])[e];
         if (!wait_phase_warp(&c.s_full, gt & 1, wc)) { ok = false; break; }
         tc_fence_after();
         const int i0 = (it.i_start + t % it.per_head) * kT + 64 * hsel;
         // causal: key j is visible to query i0 + e iff e >= j - L + Sq - i0
         const int qlo = p.causal ? j - it.L + p.Sq - i0 : -1;
-        const float2* nlq = reinterpret_cast<const float2*>(&c.nlse[s][64 * hsel]);
-        const float2* ndq = reinterpret_cast<const float2*>(&c.ndel[s][64 * hsel]);
+        const float2* nlq = reinterpret_cast<const float2*>(nlv);
+        const float4* ndg = reinterpret_cast<const float4*>(&c.ndel[s][64 * hsel]);
         const uint32_t ts = t_s + lane_off + 64 * hsel;
         float pr[64];
         tmem_ld64(ts, reinterpret_cast<uint32_t*>(pr));
@@ -845,23 +853,37 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         tc_fence_before();
         mbar_arrive(&c.p_ready);
         // dS^T = P^T * (dP^T - delta), over dP^T's first columns of this half; a key past
-        // the valid length may turn NaN here, but its dK row is written as zeros
+        // the valid length may turn NaN here, but its dK row is written as zeros. The
+        // -delta of each 32-column half is fetched ahead of its use, as above.
+        float4 ndv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ndv[e] = ndg[e];
         if (!wait_phase_warp(&c.dp_full, gt & 1, wc)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tdp = t_dp + lane_off + 64 * hsel;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
+          float4 ndn[8];
+          if (half == 0) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ndn[e] = ndg[8 + e];
+          }
           float dp[32];
           tmem_ld32(tdp + 32 * half, reinterpret_cast<uint32_t*>(dp));
           uint32_t dd[16];
+          const float2* ndq = reinterpret_cast<const float2*>(ndv);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int c0 = 32 * half + 2 * e;
-            const float2 d = f2mul(f2add(make_float2(dp[2 * e], dp[2 * e + 1]), ndq[c0 / 2]),
+            const float2 d = f2mul(f2add(make_float2(dp[2 * e], dp[2 * e + 1]), ndq[e]),
                                    make_float2(pr[c0], pr[c0 + 1]));
             dd[e] = pack_bf16x2(d.x, d.y);
           }
           tmem_st16(tdp + 16 * half, dd);
+          if (half == 0) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ndv[e] = ndn[e];
+          }
         }
         tmem_wait_st();
         tc_fence_before();
@@ -980,7 +1002,7 @@ template <int D, int NK, int NV>
 constexpr size_t dq_smem() {
   return 1024 + (size_t)(2 + NK + NV) * kT * D * 2 + sizeof(DqCtl<NK, NV>);
 }
-// stages: as many as fit in 227 KB next to the single-buffered tiles
+// dK/dV: Q/dO stages of 128 queries, as many as fit in 227 KB next to K and V
 template <int D>
 constexpr int kStages = D == 64 ? 5 : 2;
 static_assert(dkdv_smem<64, kStages<64>>() <= 232448 && dkdv_smem<128, kStages<128>>() <= 232448,
