@@ -56,6 +56,21 @@ def _stamp(extra_flags) -> str:
     return h.hexdigest()
 
 
+def source_digest() -> str:
+    """Hash of the CUDA sources and headers by relative path and content only (the same on
+    any machine and checkout path): the key under which measured per-kernel figures, such
+    as DRAM traffic, are recorded."""
+    h = hashlib.sha256()
+    files = _sources() + sorted(glob.glob(os.path.join(CSRC, "*.h")) +
+                                glob.glob(os.path.join(CSRC, "*.cuh")) +
+                                glob.glob(os.path.join(ROOT, "include", "*.h")))
+    for f in sorted(files, key=lambda p: os.path.relpath(p, ROOT)):
+        h.update(os.path.relpath(f, ROOT).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     """Compile and link libattn.so; returns its path."""
     os.makedirs(BUILD, exist_ok=True)

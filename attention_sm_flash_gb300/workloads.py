@@ -86,6 +86,10 @@ WORKLOADS = {
                     lens_lo=1560, lens_hi=32760),
     "c5": Workload("c5", "dit_cross_sq32760_skv512_valid300_h40_d128", 1, 40, 40, 32760, 512,
                    128, "bf16", False, 20265, lens_kind="fixed", lens_fixed=300),
+    # the report's own attention-timing shape (480 x 832 video, frame 27: 4680 queries over
+    # a 28080-token KV cache, 40 heads): context for its FA3 figure, not a graded workload
+    "ctx": Workload("ctx", "page_dit_self_q4680_k28080_h40_d128", 1, 40, 40, 4680, 28080, 128,
+                    "bf16", False, 20268, qk_factor=0.5),
     # profiling cases: the same kernels at sizes an ncu capture replays quickly, with
     # inputs still larger than L2 (129 MB)
     "p_self": Workload("p_self", "profile_self_s16384_h16_d128", 1, 16, 16, 16384, 16384, 128,

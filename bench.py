@@ -243,7 +243,7 @@ def traffic_for(kernel_key):
     if not os.path.exists(path):
         return None
     from attention_sm_flash_gb300 import build as libbuild
-    stamp = libbuild._stamp(())[:16]
+    stamp = libbuild.source_digest()
     with open(path) as f:
         for line in f:
             parts = line.split()
