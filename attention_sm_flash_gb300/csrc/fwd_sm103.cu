@@ -7,17 +7,21 @@
 // are padding and never enter a result ("LingBot full-pipeline analysis report", section
 // "same-GPU FA2/FA3 hardware comparison").
 //
-// One persistent CTA per SM (384 threads) loops over work items of 256 query rows of one
-// (batch, head), taken in a longest-first order:
+// One persistent CTA per SM (384 threads) loops over work items of 128 query rows (one Q
+// tile) of one (batch, head), taken in a longest-first order:
 //   warp 0      TMA producer: a ring of Q tiles (the next item's Q is prefetched), and a
 //               ring of K/V tiles of 128 keys;
-//   warps 1, 2  MMA issuers (one thread each, one per Q tile): S_t = Q_t K^T into TMEM,
-//               O_t += P_t V from TMEM;
-//   warp 3      zeroes the padding rows of partial V tiles;
-//   warps 4-7   softmax of Q tile 0 (128 rows, one row per thread);
-//   warps 8-11  softmax of Q tile 1.
-// TMEM (512 columns): S0 | S1 | O0 | O1. The softmax reads its S row, writes P (bf16)
-// over the first half of the same columns, and the PV MMA reads P from there. A row's
+//   warp 1      issues S = Q K^T into TMEM (one thread);
+//   warp 2      zeroes the padding rows of partial V tiles;
+//   warp 3      issues O += P V with P from TMEM (one thread);
+//   warps 4-11  softmax, two threads per row (64 key columns each).
+// TMEM (512 columns): S double buffer | P | O. S(j + 2) is computed into S(j)'s buffer as
+// soon as the softmax has read S(j) into registers, so the softmax of tile j + 1 starts
+// the moment tile j is done and the S products run under the softmax; P has its own
+// columns, so no S product waits for a PV product, and the softmax only waits for
+// PV(j - 1) before it overwrites P. (Two Q tiles per CTA with P written over S, the
+// layout that fits two tiles in TMEM, measured 40 % tensor-pipe use: each S waited for
+// the previous PV of its tile, and the two tiles' chains ran in lockstep.) A row's
 // running max is only raised (and O, l rescaled) when it grows by more than 2^8, which
 // leaves the result exact while skipping almost every rescale.
 //
@@ -42,15 +46,9 @@ using namespace sm103;
 
 constexpr int kBM = 128;         // rows of a Q tile (TMEM lanes)
 constexpr int kBN = 128;         // keys of a K/V tile
-constexpr int kItemRows = 2 * kBM;
-constexpr int kThreads = 384;    // warps 0-3: producer, 2 MMA issuers, V fixer; 4-7, 8-11: softmax
-// Register split (setmaxnreg): the block launches with kLaunchRegs a thread; warpgroup 0
-// then drops to kRegsLow and the two softmax warpgroups rise to kRegsHigh. The raise
-// draws on the registers the block was launched with, so the split must fit in them.
-constexpr int kLaunchRegs = 168;
-constexpr int kRegsLow = 112;
-constexpr int kRegsHigh = 192;
-static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs, "register split");
+constexpr int kItemRows = kBM;
+constexpr int kThreads = 384;    // warps 0-3: producer, S issuer, V fixer, PV issuer; 4-11: softmax
+constexpr int kSoftThreads = 256;
 constexpr int kMaxSortedHeads = 64;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows > 2^8
 
@@ -72,14 +70,19 @@ struct FwdParams {
   uint32_t fault;    // test-only: bit 0 = the producer of CTA 0 skips its first K load
 };
 
-template <int NQ, int NST>
+template <int NQ, int NK, int NV>
 struct FwdCtl {
   uint64_t mma_final[2];
   uint64_t q_full[NQ], q_empty[NQ];
-  uint64_t kv_full[NST], kv_empty[NST], kv_fixed[NST], fix_req[NST];
-  uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+  uint64_t k_full[NK], k_empty[NK];
+  uint64_t v_full[NV], v_empty[NV], v_fixed[NV], fix_req[NV];
+  // per S/P buffer; a parity wait only tells apart phases one apart, and the softmax
+  // can run two tiles ahead of the issuer, so P readiness is tracked per P buffer
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free;
+  uint64_t xfull[4], xdone[4];  // per lane quadrant: the two threads of a row trade a value
   uint32_t tmem_base;
   int abort;
+  float xbuf[2][kBM];           // [half][row]
   int n_sorted;
   int sorted[kMaxSortedHeads];
   int lens[kMaxSortedHeads];
@@ -87,8 +90,7 @@ struct FwdCtl {
 
 struct Item {
   int b, h, kvh, q0, L;
-  int n[2];   // K/V tiles each Q tile visits
-  int nload;  // K/V tiles loaded (max of n)
+  int n;  // K/V tiles the Q tile visits
 };
 
 __device__ __forceinline__ int clamp_len(int L, int Skv) { return L < 0 ? 0 : (L > Skv ? Skv : L); }
@@ -133,23 +135,13 @@ __device__ __forceinline__ Item decode_item(int idx, const FwdParams& p, const C
   it.kvh = h / g;
   it.q0 = qb * kItemRows;
   it.L = p.kv_lens ? clamp_len(__ldg(p.kv_lens + b * p.Hkv + it.kvh), p.Skv) : p.Skv;
-  it.nload = 0;
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int i0 = it.q0 + t * kBM;
-    int n = 0;
-    if (i0 < p.Sq) {
-      int kmax = it.L;
-      if (p.causal) {
-        const int ilast = min(i0 + kBM - 1, p.Sq - 1);
-        kmax = min(it.L, ilast + it.L - p.Sq + 1);
-      }
-      kmax = max(kmax, 0);
-      n = (kmax + kBN - 1) / kBN;
-    }
-    it.n[t] = n;
-    it.nload = max(it.nload, n);
+  int kmax = it.L;
+  if (p.causal) {
+    const int ilast = min(it.q0 + kBM - 1, p.Sq - 1);
+    kmax = min(it.L, ilast + it.L - p.Sq + 1);
   }
+  kmax = max(kmax, 0);
+  it.n = (kmax + kBN - 1) / kBN;
   return it;
 }
 
@@ -165,9 +157,7 @@ __device__ __forceinline__ int pv_steps(int j, int L) {
   return (valid + 15) / 16;
 }
 
-template <int D, int NQ, int NST>
-// 12 warps, 3 per sub-partition (16K registers each): launched with <= 168 registers a
-// thread, then rebalanced with setmaxnreg (see kRegsLow / kRegsHigh).
+template <int D, int NQ, int NK, int NV>
 __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
   constexpr int kQTile = kBM * D * 2;     // bytes of a Q tile
   constexpr int kKVTile = kBN * D * 2;    // bytes of a K or V tile
@@ -176,14 +166,18 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
   constexpr int kChunks = D / 64;
   constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
   constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);
-  using Ctl = FwdCtl<NQ, NST>;
+  // TMEM columns: S double buffer [0, 256), P double buffer [256, 384) (bf16 pairs),
+  // O [384, 384 + D); tile g uses S and P buffer g % 2
+  constexpr uint32_t kColP = 256, kColO = 384;
+  using Ctl = FwdCtl<NQ, NK, NV>;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;                    // NQ tile slots
-  uint8_t* sKV = smem + NQ * kQTile;     // NST tile slots
-  Ctl& c = *reinterpret_cast<Ctl*>(sKV + NST * kKVTile);
+  uint8_t* sK = smem + NQ * kQTile;      // NK tile slots
+  uint8_t* sV = sK + NK * kKVTile;       // NV tile slots
+  Ctl& c = *reinterpret_cast<Ctl*>(sV + NV * kKVTile);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -195,17 +189,26 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
       mbar_init(&c.q_full[s], 1);
       mbar_init(&c.q_empty[s], 1);
     }
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(&c.kv_full[s], 1);
-      mbar_init(&c.kv_empty[s], 2);  // released by both MMA issuers
-      mbar_init(&c.kv_fixed[s], 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(&c.k_full[s], 1);
+      mbar_init(&c.k_empty[s], 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(&c.v_full[s], 1);
+      mbar_init(&c.v_empty[s], 1);
+      mbar_init(&c.v_fixed[s], 1);
       mbar_init(&c.fix_req[s], 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(&c.s_full[t], 1);
-      mbar_init(&c.p_full[t], kBM);
-      mbar_init(&c.o_done[t], 1);
-      mbar_init(&c.o_free[t], kBM);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&c.s_full[b], 1);
+      mbar_init(&c.s_free[b], kSoftThreads);
+      mbar_init(&c.pv_done[b], 1);
+      mbar_init(&c.p_full[b], kSoftThreads);
+    }
+    mbar_init(&c.o_free, kSoftThreads);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&c.xfull[q], 64);
+      mbar_init(&c.xdone[q], 64);
     }
     c.abort = 0;
     fence_mbar_init();
@@ -243,242 +246,285 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
   const uint32_t tmem = c.tmem_base;
   WaitCtl wc{&c.abort, p.err, p.timeout_ns};
 
-  if (warp < 4) {
-    // warpgroup 0 hands registers to the softmax warpgroups
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsLow) : "memory");
-    if (warp == 0) {
-      // ------------------------------------------------------------- TMA producer
+  if (warp == 0) {
+    // ------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&p.tm_q);
+      tma_prefetch_map(&p.tm_k);
+      tma_prefetch_map(&p.tm_v);
+    }
+    // K_j is read by S(j), which runs up to two tiles ahead of PV(j); so K is loaded two
+    // tiles ahead of V and kept on its own ring, freed as soon as S(j) completes
+    uint32_t kpos = 0, vpos = 0, qs = 0, q_par = 0;
+    uint32_t k_iss = 0, k_last = 0, v_iss = 0, v_last = 0;  // per slot: a load was issued / its parity
+    uint32_t q_issued = 0, q_last = 0;                      // per Q slot
+    bool ok = true, first = true;
+    for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+      const Item it = decode_item(idx, p, c);
+      if (it.n == 0) continue;
+      if (!wait_phase_warp(&c.q_empty[qs], q_par ^ 1, wc)) { ok = false; break; }
       if (lane == 0) {
-        tma_prefetch_map(&p.tm_q);
-        tma_prefetch_map(&p.tm_k);
-        tma_prefetch_map(&p.tm_v);
+        mbar_expect_tx(&c.q_full[qs], kQTile);
+        for (int ch = 0; ch < kChunks; ++ch)
+          tma_load_4d(sQ + qs * kQTile + ch * kQChunk, &p.tm_q, &c.q_full[qs], ch * 64, it.h, it.q0, it.b);
       }
-      uint32_t slot = 0, ring_par = 0, qs = 0, q_par = 0;
-      uint32_t issued = 0, last_par = 0;    // per K/V slot: a load was issued / its parity
-      uint32_t q_issued = 0, q_last = 0;    // per Q slot
-      bool ok = true, first = true;
-      for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-        const Item it = decode_item(idx, p, c);
-        if (it.nload == 0) continue;
-        for (int t = 0; t < 2; ++t) {
-          if (!wait_phase_warp(&c.q_empty[qs], q_par ^ 1, wc)) { ok = false; break; }
+      q_issued |= 1u << qs;
+      q_last = (q_last & ~(1u << qs)) | (q_par << qs);
+      if (++qs == NQ) { qs = 0; q_par ^= 1; }
+      for (int step = 0; ok && step < it.n + 2; ++step) {
+        if (step < it.n) {
+          const int j = step;
+          const uint32_t ks = kpos % NK, kpar = (kpos / NK) & 1;
+          if (!wait_phase_warp(&c.k_empty[ks], kpar ^ 1, wc)) { ok = false; break; }
+          const bool skip = (p.fault & 1u) && blockIdx.x == 0 && first && j == 0;
+          if (!skip) {
+            if (lane == 0) {
+              mbar_expect_tx(&c.k_full[ks], kKVTile);
+              for (int ch = 0; ch < kChunks; ++ch)
+                tma_load_4d(sK + ks * kKVTile + ch * kKVChunk, &p.tm_k, &c.k_full[ks], ch * 64, it.kvh,
+                            j * kBN, it.b);
+            }
+            k_iss |= 1u << ks;
+            k_last = (k_last & ~(1u << ks)) | (kpar << ks);
+          }
+          ++kpos;
+        }
+        if (step >= 2) {
+          const int j = step - 2;
+          const uint32_t vs = vpos % NV, vpar = (vpos / NV) & 1;
+          if (!wait_phase_warp(&c.v_empty[vs], vpar ^ 1, wc)) { ok = false; break; }
           if (lane == 0) {
-            mbar_expect_tx(&c.q_full[qs], kQTile);
+            mbar_expect_tx(&c.v_full[vs], kKVTile);
             for (int ch = 0; ch < kChunks; ++ch)
-              tma_load_4d(sQ + qs * kQTile + ch * kQChunk, &p.tm_q, &c.q_full[qs], ch * 64, it.h,
-                          it.q0 + t * kBM, it.b);
+              tma_load_4d(sV + vs * kKVTile + ch * kKVChunk, &p.tm_v, &c.v_full[vs], ch * 64, it.kvh,
+                          j * kBN, it.b);
           }
-          q_issued |= 1u << qs;
-          q_last = (q_last & ~(1u << qs)) | (q_par << qs);
-          if (++qs == NQ) { qs = 0; q_par ^= 1; }
+          v_iss |= 1u << vs;
+          v_last = (v_last & ~(1u << vs)) | (vpar << vs);
+          // a V tile with padding rows: warp 2 zeroes them once the tile has landed
+          if (needs_fix(j, it.L, p.Skv) && lane == 0) mbar_arrive(&c.fix_req[vs]);
+          ++vpos;
         }
-        for (int j = 0; ok && j < it.nload; ++j) {
-          for (int kv = 0; kv < 2; ++kv) {
-            if (!wait_phase_warp(&c.kv_empty[slot], ring_par ^ 1, wc)) { ok = false; break; }
-            const bool skip = (p.fault & 1u) && blockIdx.x == 0 && first && j == 0 && kv == 0;
-            if (!skip) {
-              if (lane == 0) {
-                mbar_expect_tx(&c.kv_full[slot], kKVTile);
-                for (int ch = 0; ch < kChunks; ++ch)
-                  tma_load_4d(sKV + slot * kKVTile + ch * kKVChunk, kv == 0 ? &p.tm_k : &p.tm_v,
-                              &c.kv_full[slot], ch * 64, it.kvh, j * kBN, it.b);
-              }
-              issued |= 1u << slot;
-              last_par = (last_par & ~(1u << slot)) | (ring_par << slot);
-            }
-            // a V tile with padding rows: warp 3 zeroes them once the tile has landed
-            if (kv == 1 && needs_fix(j, it.L, p.Skv) && lane == 0) mbar_arrive(&c.fix_req[slot]);
-            if (++slot == NST) { slot = 0; ring_par ^= 1; }
-          }
-        }
-        first = false;
       }
-      // every copy this CTA started lands before its shared memory can go away (after an
-      // abort the consumers may never have waited for them)
-      for (int s = 0; s < NST; ++s)
-        if (issued & (1u << s)) wait_phase_teardown(&c.kv_full[s], (last_par >> s) & 1, 200000000ull);
-      for (int s = 0; s < NQ; ++s)
-        if (q_issued & (1u << s)) wait_phase_teardown(&c.q_full[s], (q_last >> s) & 1, 200000000ull);
-    } else if (warp == 1 || warp == 2) {
-      // ------------------------------------------------------------- MMA issuers
-      // one issuing thread per Q tile (warp 1: tile 0, warp 2: tile 1), so that each
-      // tile's S / PV chain advances as soon as its own softmax is done; both threads
-      // release every K/V slot (kv_empty counts two arrivals)
-      if (lane == 0) {
-        const int t = warp - 1;
-        const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
-        // K-major Q and K tiles (128-byte rows, 8-row groups 1024 bytes apart); MN-major V
-        // (64-column chunks kKVChunk bytes apart)
-        const uint64_t desc_q0 = smem_desc_sw128(sQa, 16, 1024);
-        const uint64_t desc_k0 = smem_desc_sw128(sKVa, 16, 1024);
-        const uint64_t desc_v0 = smem_desc_sw128(sKVa, kKVChunk, 1024);
-        // ring positions: the k-th loaded item's Q tile t is Q position 2 k + t; its K/V
-        // tile j is at 2 (kbase + j) (K) and 2 (kbase + j) + 1 (V); a position's slot is
-        // pos % N and its phase parity (pos / N) % 2
-        uint32_t kbase = 0, qpos = t, fix_par = 0, pv = 0, pc = 0, ic = 0;
-        bool ok = true;
-        for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-          const Item it = decode_item(idx, p, c);
-          if (it.nload == 0) continue;
-          const int nt = t == 0 ? it.n[0] : it.n[1];
-          const uint32_t qslot = qpos % NQ;
-          if (!wait_phase(&c.q_full[qslot], (qpos / NQ) & 1, wc)) { ok = false; break; }
-          qpos += 2;
-          tc_fence_after();
-          if (nt == 0) mma_commit(&c.q_empty[qslot]);  // never read: free at once
-          for (int j = 0; ok && j < it.nload; ++j) {
-            const uint32_t kpos = 2 * (kbase + j), vpos = kpos + 1;
-            const uint32_t ks = kpos % NST, vs = vpos % NST;
-            // S_t(j) = Q_t K_j^T; S_t's columns hold P_t(j - 1) until PV_t(j - 1) completes
-            if (!wait_phase(&c.kv_full[ks], (kpos / NST) & 1, wc)) { ok = false; break; }
-            if (j < nt) {
-              if (pv > 0 && !wait_phase(&c.o_done[t], (pv - 1) & 1, wc)) { ok = false; break; }
-              tc_fence_after();
-              const uint64_t a0 = desc_q0 + ((qslot * kQTile) >> 4);
-              const uint64_t b0 = desc_k0 + ((ks * kKVTile) >> 4);
-  #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                mma_ss(tmem + t * 128, a0 + (((kk / 4) * kQChunk + (kk % 4) * 32) >> 4),
-                       b0 + (((kk / 4) * kKVChunk + (kk % 4) * 32) >> 4), kIdescS, kk > 0 ? 1u : 0u);
-              }
-              mma_commit(&c.s_full[t]);
-              if (j == nt - 1) mma_commit(&c.q_empty[qslot]);  // last read of Q_t
-            }
-            mma_commit(&c.kv_empty[ks]);
-            // O_t += P_t(j) V_j
-            if (needs_fix(j, it.L, p.Skv)) {
-              if (!wait_phase(&c.kv_fixed[vs], (fix_par >> vs) & 1, wc)) { ok = false; break; }
-              fix_par ^= 1u << vs;
-            } else if (!wait_phase(&c.kv_full[vs], (vpos / NST) & 1, wc)) {
-              ok = false;
-              break;
-            }
-            if (j < nt) {
-              if (!wait_phase(&c.p_full[t], pc & 1, wc)) { ok = false; break; }
-              ++pc;
-              if (j == 0 && !wait_phase(&c.o_free[t], (ic & 1) ^ 1, wc)) { ok = false; break; }
-              tc_fence_after();
-              const int steps = pv_steps(j, it.L);
-              const uint64_t b0 = desc_v0 + ((vs * kKVTile) >> 4);
-  #pragma unroll
-              for (int kk = 0; kk < kBN / 16; ++kk) {
-                if (kk < steps)
-                  mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, b0 + ((kk * 16 * 128) >> 4),
-                         kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-              }
-              mma_commit(&c.o_done[t]);
-              ++pv;
-            }
-            mma_commit(&c.kv_empty[vs]);
-          }
-          if (!ok) break;
-          kbase += it.nload;
-          if (nt > 0) ++ic;
-        }
-        // every MMA this thread issued must finish before the TMEM is freed
-        mma_commit(&c.mma_final[t]);
-        wait_phase_teardown(&c.mma_final[t], 0, 200000000ull);
-      }
-      __syncwarp();
-    } else {
-      // -------------------------------------------------------------- V-tile fixer
-      // zeroes the padding rows (at or past the valid length) of partial V tiles, so
-      // that 0 * NaN in the PV product cannot occur; requests come from the producer
-      // in ring order (fix_req), so the fill this waits for is never ambiguous
-      uint32_t kbase = 0, fr_par = 0;
+      first = false;
+    }
+    // every copy this CTA started lands before its shared memory can go away (after an
+    // abort the consumers may never have waited for them)
+    for (int s = 0; s < NK; ++s)
+      if (k_iss & (1u << s)) wait_phase_teardown(&c.k_full[s], (k_last >> s) & 1, 200000000ull);
+    for (int s = 0; s < NV; ++s)
+      if (v_iss & (1u << s)) wait_phase_teardown(&c.v_full[s], (v_last >> s) & 1, 200000000ull);
+    for (int s = 0; s < NQ; ++s)
+      if (q_issued & (1u << s)) wait_phase_teardown(&c.q_full[s], (q_last >> s) & 1, 200000000ull);
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------- MMA issuers
+    // S(j) goes to S buffer j % 2 as soon as the softmax has read S(j - 2) out of it, so
+    // the S product of a later tile always runs while the softmax works on the current
+    // one; PV(j) follows once P(j) is written into P buffer j % 2. P has its own
+    // columns, so no S product ever waits for a PV product.
+    // warp 1 issues the S products, warp 3 the PV products: each thread's waits then
+    // block only its own product family (a wait costs hundreds of cycles while SS MMAs
+    // hold the shared-memory bandwidth)
+    const bool s_role = warp == 1;
+    if (lane == 0) {
+      const uint32_t sQa = smem_u32(sQ);
+      // K-major Q and K tiles (128-byte rows, 8-row groups 1024 bytes apart); MN-major V
+      // (64-column chunks kKVChunk bytes apart)
+      const uint64_t desc_q0 = smem_desc_sw128(sQa, 16, 1024);
+      const uint64_t desc_k0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t desc_v0 = smem_desc_sw128(smem_u32(sV), kKVChunk, 1024);
+      // ring positions: the k-th loaded item's Q tile is Q position k; its K and V tiles j
+      // are at position kbase + j of the K and the V ring; a position's slot is pos % N and
+      // its phase parity (pos / N) % 2
+      uint32_t kbase = 0, qpos = 0, fix_par = 0, gs = 0, gp = 0, ic = 0;
       bool ok = true;
+      auto issue_s = [&](uint32_t qslot, int j) -> bool {
+        const uint32_t kpos = kbase + j, ks = kpos % NK;
+        if (!wait_phase(&c.k_full[ks], (kpos / NK) & 1, wc)) return false;
+        const uint32_t b = gs & 1;
+        if (gs >= 2 && !wait_phase(&c.s_free[b], ((gs >> 1) - 1) & 1, wc)) return false;
+        tc_fence_after();
+        const uint64_t a0 = desc_q0 + ((qslot * kQTile) >> 4);
+        const uint64_t b0 = desc_k0 + ((ks * kKVTile) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + b * 128, a0 + (((kk / 4) * kQChunk + (kk % 4) * 32) >> 4),
+                 b0 + (((kk / 4) * kKVChunk + (kk % 4) * 32) >> 4), kIdescS, kk > 0 ? 1u : 0u);
+        mma_commit(&c.s_full[b]);
+        mma_commit(&c.k_empty[ks]);  // K_j is read by this product only
+        ++gs;
+        return true;
+      };
+      auto issue_pv = [&](int j, int L) -> bool {
+        const uint32_t vpos = kbase + j, vs = vpos % NV;
+        if (needs_fix(j, L, p.Skv)) {
+          if (!wait_phase(&c.v_fixed[vs], (fix_par >> vs) & 1, wc)) return false;
+          fix_par ^= 1u << vs;
+        } else if (!wait_phase(&c.v_full[vs], (vpos / NV) & 1, wc)) {
+          return false;
+        }
+        if (!wait_phase(&c.p_full[gp & 1], (gp >> 1) & 1, wc)) return false;
+        if (j == 0 && !wait_phase(&c.o_free, (ic & 1) ^ 1, wc)) return false;
+        tc_fence_after();
+        const int steps = pv_steps(j, L);
+        const uint64_t b0 = desc_v0 + ((vs * kKVTile) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          if (kk < steps)
+            mma_ts(tmem + kColO, tmem + kColP + (gp & 1) * 64 + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescPV,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&c.pv_done[gp & 1]);
+        mma_commit(&c.v_empty[vs]);
+        ++gp;
+        return true;
+      };
       for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
         const Item it = decode_item(idx, p, c);
-        if (it.nload == 0) continue;
-        for (int j = 0; j < it.nload; ++j) {
-          if (!needs_fix(j, it.L, p.Skv)) continue;
-          const uint32_t vpos = 2 * (kbase + j) + 1, vs = vpos % NST;
-          if (!wait_phase_warp(&c.fix_req[vs], (fr_par >> vs) & 1, wc)) { ok = false; break; }
-          fr_par ^= 1u << vs;
-          if (!wait_phase_warp(&c.kv_full[vs], (vpos / NST) & 1, wc)) { ok = false; break; }
-          const int r0 = it.L - j * kBN;  // first padding row (>= 1: tile j holds valid keys)
-          const int units = (kBN - r0) * kChunks * 8;
-          uint8_t* base = sKV + vs * kKVTile;
-          for (int e = lane; e < units; e += 32) {
-            const int r = r0 + e / (kChunks * 8);
-            const int rest = e % (kChunks * 8);
-            *reinterpret_cast<uint4*>(base + (rest / 8) * kKVChunk + r * 128 + (rest % 8) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&c.kv_fixed[vs]);
+        if (it.n == 0) continue;
+        const uint32_t qslot = qpos % NQ;
+        if (s_role && !wait_phase(&c.q_full[qslot], (qpos / NQ) & 1, wc)) { ok = false; break; }
+        ++qpos;
+        tc_fence_after();
+        if (s_role) {
+          // S(t) as soon as its K tile is in and the softmax has read S(t - 2)
+          for (int t = 0; ok && t < it.n; ++t) ok = issue_s(qslot, t);
+          if (!ok) break;
+          mma_commit(&c.q_empty[qslot]);  // last read of Q
+        } else {
+          // PV(t) once the softmax has written P(t)
+          for (int t = 0; ok && t < it.n; ++t) ok = issue_pv(t, it.L);
+          if (!ok) break;
         }
-        kbase += it.nload;
+        kbase += it.n;
+        ++ic;
       }
-  }
-  } else {
-    // --------------------------------------------------------------------- softmax
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegsHigh) : "memory");
-    const int t = (warp - 4) / 4;
-    const int quad = warp % 4;  // TMEM lanes a warp may touch: 32 * (warp % 4) ...
-    const int r = quad * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_off + t * 128;
-    const uint32_t tO = tmem + lane_off + 256 + t * D;
-    const bool pos_scale = p.scale_log2 > 0.f;
-    uint32_t s_cnt = 0, npv = 0;
+      // every MMA this thread issued must finish before the TMEM is freed
+      mma_commit(&c.mma_final[s_role ? 0 : 1]);
+      wait_phase_teardown(&c.mma_final[s_role ? 0 : 1], 0, 200000000ull);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // -------------------------------------------------------------- V-tile fixer
+    // zeroes the padding rows (at or past the valid length) of partial V tiles, so
+    // that 0 * NaN in the PV product cannot occur; requests come from the producer
+    // in ring order (fix_req), so the fill this waits for is never ambiguous
+    uint32_t kbase = 0, fr_par = 0;
     bool ok = true;
     for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
       const Item it = decode_item(idx, p, c);
-      const int i = it.q0 + t * kBM + r;
+      if (it.n == 0) continue;
+      for (int j = 0; j < it.n; ++j) {
+        if (!needs_fix(j, it.L, p.Skv)) continue;
+        const uint32_t vpos = kbase + j, vs = vpos % NV;
+        if (!wait_phase_warp(&c.fix_req[vs], (fr_par >> vs) & 1, wc)) { ok = false; break; }
+        fr_par ^= 1u << vs;
+        if (!wait_phase_warp(&c.v_full[vs], (vpos / NV) & 1, wc)) { ok = false; break; }
+        const int r0 = it.L - j * kBN;  // first padding row (>= 1: tile j holds valid keys)
+        const int units = (kBN - r0) * kChunks * 8;
+        uint8_t* base = sV + vs * kKVTile;
+        for (int e = lane; e < units; e += 32) {
+          const int r = r0 + e / (kChunks * 8);
+          const int rest = e % (kChunks * 8);
+          *reinterpret_cast<uint4*>(base + (rest / 8) * kKVChunk + r * 128 + (rest % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.v_fixed[vs]);
+      }
+      kbase += it.n;
+    }
+  } else if (warp >= 4) {
+    // --------------------------------------------------------------------- softmax
+    // Two threads per row: warp w reaches TMEM lanes 32 * (w % 4) .. and takes the key
+    // columns 64 h .. 64 h + 63 of each tile, h = (w - 4) / 4. The pair trades its
+    // partial row max every tile (and its partial row sum at the end) through shared
+    // memory, so both halves use the same running max; each half keeps its own part of
+    // the row sum and rescales its half of O.
+    const int quad = warp % 4;
+    const int h = (warp - 4) / 4;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tO = tmem + lane_off + kColO + h * (D / 2);
+    const bool pos_scale = p.scale_log2 > 0.f;
+    uint32_t g = 0;   // tiles processed so far (all items): S and P buffer g % 2, PV number g
+    uint32_t xc = 0;  // exchanges with the other half of the row so far
+    bool ok = true;
+    // hands `v` to the other half of the row and returns its value
+    auto trade = [&](float v, float& other) -> bool {
+      if (xc > 0 && !wait_phase_warp(&c.xdone[quad], (xc - 1) & 1, wc)) return false;
+      c.xbuf[h][r] = v;
+      mbar_arrive(&c.xfull[quad]);
+      if (!wait_phase_warp(&c.xfull[quad], xc & 1, wc)) return false;
+      other = c.xbuf[1 - h][r];
+      mbar_arrive(&c.xdone[quad]);
+      ++xc;
+      return true;
+    };
+    for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+      const Item it = decode_item(idx, p, c);
+      const int i = it.q0 + r;
       const bool row_ok = i < p.Sq;
-      __nv_bfloat16* orow = p.o + ((static_cast<int64_t>(it.b) * p.Sq + i) * p.Hq + it.h) * D;
+      __nv_bfloat16* orow = p.o + ((static_cast<int64_t>(it.b) * p.Sq + i) * p.Hq + it.h) * D + h * (D / 2);
       float* lrow = p.lse + (static_cast<int64_t>(it.b) * p.Hq + it.h) * p.Sq + i;
-      const int nt = t == 0 ? it.n[0] : it.n[1];
-      if (nt == 0) {
+      if (it.n == 0) {
         if (row_ok) {
-          for (int d = 0; d < D; d += 8)
+          for (int d = 0; d < D / 2; d += 8)
             *reinterpret_cast<uint4*>(orow + d) = make_uint4(0u, 0u, 0u, 0u);
-          *lrow = -CUDART_INF_F;
+          if (h == 0) *lrow = -CUDART_INF_F;
         }
         continue;
       }
       // visible keys of this row: [0, kend)
       const int kend = p.causal ? min(it.L, i + it.L - p.Sq + 1) : it.L;
       float m = -CUDART_INF_F, l = 0.f;
-      for (int j = 0; j < nt; ++j) {
-        if (!wait_phase_warp(&c.s_full[t], s_cnt & 1, wc)) { ok = false; break; }
-        ++s_cnt;
+      for (int j = 0; j < it.n; ++j, ++g) {
+        const uint32_t b = g & 1;
+        if (!wait_phase_warp(&c.s_full[b], (g >> 1) & 1, wc)) { ok = false; break; }
         tc_fence_after();
-        const int limit = kend - j * kBN;
-        // one TMEM round trip: the whole S row of this tile into registers
-        float s[kBN];
-        tmem_ld128(tS, reinterpret_cast<uint32_t*>(s));
-        // the row max of the scaled scores over the visible keys, 8 independent chains;
-        // for a positive scale the max of the raw scores, scaled once
+        // visible columns of this half: e < limit
+        const int limit = kend - j * kBN - 64 * h;
+        // one TMEM round trip: this half of the S row into registers, which (with the
+        // other half) frees the buffer for S(j + 2)
+        float s[64];
+        tmem_ld64(tmem + lane_off + b * 128 + 64 * h, reinterpret_cast<uint32_t*>(s));
+        tc_fence_before();
+        mbar_arrive(&c.s_free[b]);
+        // the half row max, 8 independent chains; for a positive scale the max of the raw
+        // scores, scaled once
         float mx8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx8[e] = -CUDART_INF_F;
-        const bool full = limit >= kBN;
+        const bool full = limit >= 64;
         if (pos_scale && full) {
 #pragma unroll
-          for (int e = 0; e < kBN / 2; ++e) mx8[e % 8] = max3f(mx8[e % 8], s[2 * e], s[2 * e + 1]);
+          for (int e = 0; e < 32; ++e) mx8[e % 8] = max3f(mx8[e % 8], s[2 * e], s[2 * e + 1]);
         } else {
 #pragma unroll
-          for (int e = 0; e < kBN; ++e) {
+          for (int e = 0; e < 64; ++e) {
             const float v = pos_scale ? s[e] : s[e] * p.scale_log2;
             mx8[e % 8] = fmaxf(mx8[e % 8], e < limit ? v : -CUDART_INF_F);
           }
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float mxh = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        float mxo;
+        if (!trade(mxh, mxo)) { ok = false; break; }
+        const float mx = fmaxf(mxh, mxo);  // the same value in both halves
         const float mnew = fmaxf(m, pos_scale ? mx * p.scale_log2 : mx);
         const bool raise = mnew > m + kRescaleThreshold;
         const bool rescale = raise && m != -CUDART_INF_F;
         // TMEM loads/stores are warp-collective: the warp rescales together, rows that
-        // need no rescale with a factor of 1. S_t(j) landed, so every earlier MMA of the
-        // issuer (PV_t(j-1)) has too and O_t holds its sum.
+        // need no rescale with a factor of 1. O holds the sum through PV(g - 1) once that
+        // product completes (rescale implies j > 0).
         if (__any_sync(0xffffffffu, rescale)) {
+          if (!wait_phase_warp(&c.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
           const float alpha = rescale ? ex2_approx(m - mnew) : 1.f;
           l *= alpha;
 #pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = 0; cc < D / 64; ++cc) {
             uint32_t ov[32];
             tmem_ld32(tO + cc * 32, ov);
 #pragma unroll
@@ -487,19 +533,21 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
           }
         }
         if (raise) m = mnew;
-        // P = 2^(s * scale * log2 e - m) in bf16 over the first half of S's columns, a
-        // quarter at a time (the fence keeps each quarter after the previous store)
+        // P = 2^(s * scale * log2 e - m) in bf16 into P buffer g % 2 (this half's 32
+        // columns), in two quarters; the first store waits until PV(g - 2) has read that
+        // buffer
         const float msub = m == -CUDART_INF_F ? 0.f : m;
+        const uint32_t tP = tmem + lane_off + kColP + b * 64 + 32 * h;
         float rs8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q2 = 0; q2 < 2; ++q2) {
           uint32_t pk[16];
-          if (q4 > 0) reg_fence32(s + q4 * 32);  // after the previous quarter's store
+          if (q2 > 0) reg_fence32(s + q2 * 32);  // after the previous quarter's store
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const int c0 = q4 * 32 + 2 * e;
+            const int c0 = q2 * 32 + 2 * e;
             float x0, x1;
             ffma2_bcast(x0, x1, s[c0], s[c0 + 1], p.scale_log2, -msub);
             if (!full) {
@@ -511,21 +559,29 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
             fadd2_acc(rs8[2 * (e % 4)], rs8[2 * (e % 4) + 1], p0, p1);
             pk[e] = pack_bf16x2(p0, p1);
           }
-          tmem_st16(tS + q4 * 16, pk);
+          if (q2 == 0 && g >= 2) {
+            if (!wait_phase_warp(&c.pv_done[b], ((g >> 1) - 1) & 1, wc)) { ok = false; break; }
+            tc_fence_after();
+          }
+          tmem_st16(tP + q2 * 16, pk);
         }
+        if (!ok) break;
         l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&c.p_full[t]);
-        ++npv;
+        mbar_arrive(&c.p_full[b]);
       }
       if (!ok) break;
-      // epilogue: O / l and LSE
-      if (!wait_phase_warp(&c.o_done[t], (npv - 1) & 1, wc)) { ok = false; break; }
+      // epilogue: the row sum of both halves (added in a fixed order), then O / l and
+      // LSE once PV(g - 1), the item's last, has completed
+      float lo;
+      if (!trade(l, lo)) { ok = false; break; }
+      const float lt = h == 0 ? l + lo : lo + l;
+      if (!wait_phase_warp(&c.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, wc)) { ok = false; break; }
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t ov[32];
         tmem_ld32(tO + cc * 32, ov);
         if (row_ok) {
@@ -538,9 +594,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
           for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
       }
-      if (row_ok) *lrow = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+      if (row_ok && h == 0) *lrow = lt > 0.f ? (m + __log2f(lt)) * 0.69314718055994531f : -CUDART_INF_F;
       tc_fence_before();
-      mbar_arrive(&c.o_free[t]);
+      mbar_arrive(&c.o_free);
     }
   }
 
@@ -554,9 +610,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
 }
 
 // ---------------------------------------------------------------------- host side
-template <int D, int NQ, int NST>
+template <int D, int NQ, int NK, int NV>
 constexpr size_t fwd_smem_bytes() {
-  return 1024 + (size_t)NQ * kBM * D * 2 + (size_t)NST * kBN * D * 2 + sizeof(FwdCtl<NQ, NST>);
+  return 1024 + (size_t)NQ * kBM * D * 2 + (size_t)(NK + NV) * kBN * D * 2 + sizeof(FwdCtl<NQ, NK, NV>);
 }
 
 constexpr int kMaxDev = 64;
@@ -564,29 +620,22 @@ std::mutex g_mu;
 int g_num_sms[kMaxDev] = {};
 bool g_attr_set[kMaxDev][2] = {};
 
-template <int D, int NQ, int NST>
+template <int D, int NQ, int NK, int NV>
 cudaError_t launch(const FwdParams& prm, int dev, cudaStream_t s) {
-  constexpr size_t smem = fwd_smem_bytes<D, NQ, NST>();
+  constexpr size_t smem = fwd_smem_bytes<D, NQ, NK, NV>();
   static_assert(smem <= 232448, "shared memory per block");
   {
     std::lock_guard<std::mutex> lk(g_mu);
     const int which = D == 64 ? 0 : 1;
     if (!g_attr_set[dev][which]) {
-      // the register split is only safe if the block launches with enough registers:
-      // a raise that the launch allocation cannot cover would wait forever
-      cudaFuncAttributes fa;
-      cudaError_t e = cudaFuncGetAttributes(&fa, fwd_sm103_kernel<D, NQ, NST>);
-      if (e != cudaSuccess) return e;
-      if (fa.numRegs * kThreads < 128 * kRegsLow + 256 * kRegsHigh || fa.numRegs > kLaunchRegs)
-        return cudaErrorInvalidConfiguration;
-      e = cudaFuncSetAttribute(fwd_sm103_kernel<D, NQ, NST>,
+      cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D, NQ, NK, NV>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
       g_attr_set[dev][which] = true;
     }
   }
   const int grid = prm.n_items < g_num_sms[dev] ? prm.n_items : g_num_sms[dev];
-  fwd_sm103_kernel<D, NQ, NST><<<grid, kThreads, smem, s>>>(prm);
+  fwd_sm103_kernel<D, NQ, NK, NV><<<grid, kThreads, smem, s>>>(prm);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -679,8 +728,8 @@ cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
     if (g_fault_next != 0 && g_fault_timeout_ns != 0) prm.timeout_ns = g_fault_timeout_ns;
     g_fault_next = 0;
   }
-  if (p.D == 64) return launch<64, 4, 8>(prm, dev, s);
-  return launch<128, 3, 4>(prm, dev, s);
+  if (p.D == 64) return launch<64, 3, 5, 4>(prm, dev, s);
+  return launch<128, 2, 3, 2>(prm, dev, s);
 }
 
 }  // namespace attn
