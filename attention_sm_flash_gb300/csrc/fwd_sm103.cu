@@ -54,6 +54,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max g
 
 struct FwdParams {
   CUtensorMap tm_q;
+  CUtensorMap tm_o;  // O, same layout and box as Q (the epilogue's tile stores)
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   __nv_bfloat16* o;
@@ -80,6 +81,7 @@ struct FwdCtl {
   // can run two tiles ahead of the issuer, so P readiness is tracked per P buffer
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free;
   uint64_t xfull[4], xdone[4];  // per lane quadrant: the two threads of a row trade a value
+  uint64_t o_staged, stage_free;  // the O staging tile: written by the softmax / read by TMA
   uint32_t tmem_base;
   int abort;
   float xbuf[2][kBM];           // [half][row]
@@ -146,7 +148,8 @@ __device__ __forceinline__ Item decode_item(int idx, const FwdParams& p, const C
 }
 
 // Whether K/V tile j holds in-bounds rows at or past the valid length (padding that may
-// hold anything, even NaN): such a V tile gets those rows zeroed before the PV product.
+// hold anything, even NaN): such a V tile gets the padding rows that the PV product reads
+// zeroed before it.
 __device__ __forceinline__ bool needs_fix(int j, int L, int Skv) {
   return min(Skv, (j + 1) * kBN) > L;
 }
@@ -177,7 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
   uint8_t* sQ = smem;                    // NQ tile slots
   uint8_t* sK = smem + NQ * kQTile;      // NK tile slots
   uint8_t* sV = sK + NK * kKVTile;       // NV tile slots
-  Ctl& c = *reinterpret_cast<Ctl*>(sV + NV * kKVTile);
+  uint8_t* sO = sV + NV * kKVTile;       // O staging tile (SW128 layout, as Q)
+  Ctl& c = *reinterpret_cast<Ctl*>(sO + kQTile);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -210,6 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
       mbar_init(&c.xfull[q], 64);
       mbar_init(&c.xdone[q], 64);
     }
+    mbar_init(&c.o_staged, kSoftThreads);
+    mbar_init(&c.stage_free, 1);
     c.abort = 0;
     fence_mbar_init();
   }
@@ -421,7 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
         fr_par ^= 1u << vs;
         if (!wait_phase_warp(&c.v_full[vs], (vpos / NV) & 1, wc)) { ok = false; break; }
         const int r0 = it.L - j * kBN;  // first padding row (>= 1: tile j holds valid keys)
-        const int units = (kBN - r0) * kChunks * 8;
+        // the PV product reads whole 16-key steps up to the last valid key: only padding
+        // rows inside that last step are read, and only they are zeroed
+        const int r1 = pv_steps(j, it.L) * 16;
+        const int units = (r1 - r0) * kChunks * 8;
         uint8_t* base = sV + vs * kKVTile;
         for (int e = lane; e < units; e += 32) {
           const int r = r0 + e / (kChunks * 8);
@@ -450,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
     const bool pos_scale = p.scale_log2 > 0.f;
     uint32_t g = 0;   // tiles processed so far (all items): S and P buffer g % 2, PV number g
     uint32_t xc = 0;  // exchanges with the other half of the row so far
+    uint32_t ic_s = 0;  // items with tiles finished (O staging tile uses)
     bool ok = true;
     // hands `v` to the other half of the row and returns its value
     auto trade = [&](float v, float& other) -> bool {
@@ -580,24 +590,48 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
       if (!wait_phase_warp(&c.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, wc)) { ok = false; break; }
       tc_fence_after();
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      // O goes out through shared memory and TMA tile stores: written straight from the
+      // registers, each thread's row slice would be 16-byte stores 32 rows apart. The
+      // staging tile is free once the previous item's store has read it.
+      if (!wait_phase_warp(&c.stage_free, (ic_s & 1) ^ 1, wc)) { ok = false; break; }
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t ov[32];
         tmem_ld32(tO + cc * 32, ov);
-        if (row_ok) {
-          uint32_t pk[16];
+        uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        for (int e = 0; e < 4; ++e) {
+          // columns col .. col + 7: 64-column chunk col / 64, 16-byte unit of its 128-byte
+          // row (col % 64) / 8, placed with the 128-byte swizzle of the tensor map
+          const int col = h * (D / 2) + cc * 32 + e * 8;
+          const int u = (col & 63) >> 3;
+          *reinterpret_cast<uint4*>(sO + (col >> 6) * (kBM * 128) + r * 128 + ((u ^ (r & 7)) * 16)) =
+              make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
       }
-      if (row_ok && h == 0) *lrow = lt > 0.f ? (m + __log2f(lt)) * 0.69314718055994531f : -CUDART_INF_F;
       tc_fence_before();
-      mbar_arrive(&c.o_free);
+      mbar_arrive(&c.o_free);  // O's columns may be overwritten
+      fence_proxy_async_smem();
+      mbar_arrive(&c.o_staged);
+      if (row_ok && h == 0) *lrow = lt > 0.f ? (m + __log2f(lt)) * 0.69314718055994531f : -CUDART_INF_F;
+      if (warp == 4) {
+        if (!wait_phase_warp(&c.o_staged, ic_s & 1, wc)) { ok = false; break; }
+        if (lane == 0) {
+#pragma unroll
+          for (int ch = 0; ch < D / 64; ++ch) tma_store_4d(&p.tm_o, sO + ch * (kBM * 128), ch * 64, it.h, it.q0, it.b);
+          tma_store_commit();
+          tma_store_wait_read();
+          mbar_arrive(&c.stage_free);
+        }
+        __syncwarp();
+      }
+      ++ic_s;
     }
+    // the last stores complete before the CTA exits
+    if (warp == 4 && lane == 0) tma_store_wait_all();
   }
 
   // ---------------------------------------------------------------------- teardown
@@ -612,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
 // ---------------------------------------------------------------------- host side
 template <int D, int NQ, int NK, int NV>
 constexpr size_t fwd_smem_bytes() {
-  return 1024 + (size_t)NQ * kBM * D * 2 + (size_t)(NK + NV) * kBN * D * 2 + sizeof(FwdCtl<NQ, NK, NV>);
+  return 1024 + (size_t)(NQ + 1) * kBM * D * 2 + (size_t)(NK + NV) * kBN * D * 2 + sizeof(FwdCtl<NQ, NK, NV>);
 }
 
 constexpr int kMaxDev = 64;
@@ -701,6 +735,7 @@ cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
   // with no keys the K/V maps are never used; describe q so that encoding succeeds
   const bool no_keys = p.Skv == 0;
   if (!make_bshd_map(&prm.tm_q, p.q, p.B, p.Sq, p.Hq, p.D, kBM) ||
+      !make_bshd_map(&prm.tm_o, p.o, p.B, p.Sq, p.Hq, p.D, kBM) ||
       !make_bshd_map(&prm.tm_k, no_keys ? p.q : p.k, p.B, no_keys ? p.Sq : p.Skv,
                 no_keys ? p.Hq : p.Hkv, p.D, kBN) ||
       !make_bshd_map(&prm.tm_v, no_keys ? p.q : p.v, p.B, no_keys ? p.Sq : p.Skv,
@@ -729,7 +764,7 @@ cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
     g_fault_next = 0;
   }
   if (p.D == 64) return launch<64, 3, 5, 4>(prm, dev, s);
-  return launch<128, 2, 3, 2>(prm, dev, s);
+  return launch<128, 2, 2, 2>(prm, dev, s);
 }
 
 }  // namespace attn
