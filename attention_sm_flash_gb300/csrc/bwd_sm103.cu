@@ -197,6 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_sm103_kernel(const __grid_
   DqCtl<NK, NV>& c = *reinterpret_cast<DqCtl<NK, NV>*>(smem + (2 + NK + NV) * kTile);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // the dK/dV kernel that follows reads none of this kernel's output: it may take each SM
+  // as soon as this kernel's CTA there exits
+  griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     mbar_init(&c.q_full, 1);
@@ -1093,7 +1096,21 @@ cudaError_t launch_bwd(const Problem& p, int dev, cudaStream_t s) {
     constexpr size_t smem = dkdv_smem<D, NST>();
     cudaError_t e = set_smem(bwd_dkdv_sm103_kernel<D, NST>, smem, dev, D == 64 ? 0 : 1);
     if (e != cudaSuccess) return e;
-    bwd_dkdv_sm103_kernel<D, NST><<<prm.n_items < sms ? prm.n_items : sms, kThreads, smem, s>>>(prm);
+    // a programmatic dependent of the dQ kernel: both only read Q, K, V, dO, LSE and delta
+    // (complete before the dQ kernel started) and write disjoint outputs, so the dK/dV
+    // CTAs need not wait for the dQ grid to finish
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(prm.n_items < sms ? prm.n_items : sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, bwd_dkdv_sm103_kernel<D, NST>, prm);
+    if (e != cudaSuccess) return e;
     count_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
