@@ -101,8 +101,8 @@ extern "C" size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk
                                           attn_dtype_t dtype) {
   if (B <= 0 || Hq <= 0 || Sq <= 0 || Hkv <= 0 || Skv < 0 || D <= 0) return 0;
   size_t n = bwd_delta_bytes(B, Hq, Sq);
-  if (Skv > 0 && Hq % Hkv == 0 && bwd_split_heads(B, Hq, Hkv, Skv, dtype))
-    n += 2 * bwd_partial_bytes(B, Hq, Skv, D);
+  const int parts = Skv > 0 ? bwd_split_parts(B, Hq, Hkv, Skv, dtype) : 0;
+  if (parts > 0) n += 2 * bwd_partial_bytes(B, Hkv, parts, Skv, D);
   return n;
 }
 
@@ -139,11 +139,11 @@ extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, c
   Problem p{};
   p.q = q; p.k = k; p.v = v; p.o_in = o; p.dout = dout; p.lse = const_cast<float*>(lse);
   p.dq = dq; p.dk = dk; p.dv = dv; p.delta = static_cast<float*>(workspace);
-  p.split = Skv > 0 && bwd_split_heads(B, Hq, Hkv, Skv, dtype) ? 1 : 0;
+  p.split = Skv > 0 ? bwd_split_parts(B, Hq, Hkv, Skv, dtype) : 0;
   if (p.split) {
     uint8_t* w = static_cast<uint8_t*>(workspace) + bwd_delta_bytes(B, Hq, Sq);
     p.part_dk = reinterpret_cast<float*>(w);
-    p.part_dv = reinterpret_cast<float*>(w + bwd_partial_bytes(B, Hq, Skv, D));
+    p.part_dv = reinterpret_cast<float*>(w + bwd_partial_bytes(B, Hkv, p.split, Skv, D));
   }
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.D = D;
   p.scale = scale; p.causal = causal; p.kv_lens = kv_lens; p.dtype = dtype;

@@ -22,9 +22,9 @@ struct Problem {
   void* dk;
   void* dv;
   float* delta;       // backward workspace: rowsum(dO * O), [B, Hq, Sq]
-  float* part_dk;     // backward workspace when the GQA group is split: fp32 [B, Skv, Hq, D]
+  float* part_dk;     // backward workspace when the GQA group is split: fp32 [B, Skv, Hkv * split, D]
   float* part_dv;
-  int split;          // 1: dK/dV per (key tile, query head) + an ordered group reduction
+  int split;          // parts per GQA group (bwd_split_parts), 0: not split
   int B, Hq, Hkv, Sq, Skv, D;
   float scale;
   int causal;
@@ -33,18 +33,28 @@ struct Problem {
   unsigned int* err;       // device error word (ATTN_DEVERR_* bits)
 };
 
-// Whether the bf16 backward splits each GQA group into one dK/dV work item per query
-// head (fp32 partial dK/dV in the workspace, then a reduction over the group in a
-// fixed order): done when (batch, kv head, 128-key tile) items alone are too few to
-// balance the GPU. A pure function of the sizes, so that the workspace query and the
-// launch agree.
-inline bool bwd_split_heads(int B, int Hq, int Hkv, int Skv, attn_dtype_t dtype) {
-  return dtype == ATTN_BF16 && Hq > Hkv && (long long)B * Hkv * ((Skv + 127) / 128) < 256;
+// Into how many parts the bf16 backward splits each GQA group's dK/dV work (0: not
+// split). A (batch, kv head, 128-key tile) work item covers the whole group; when such
+// items alone are too few to balance the GPU (under 256), each becomes `parts` items of
+// Hq / Hkv / parts consecutive query heads: the fewest parts (a divisor of the group
+// size) that give at least 256 items, else one item per query head. Each item writes an
+// fp32 partial dK/dV to the workspace and a second kernel sums a group's partials in a
+// fixed order. A pure function of the sizes, so that the workspace query and the launch
+// agree.
+inline int bwd_split_parts(int B, int Hq, int Hkv, int Skv, attn_dtype_t dtype) {
+  if (dtype != ATTN_BF16 || Hkv <= 0 || Hq <= Hkv || Hq % Hkv != 0) return 0;
+  const long long items = (long long)B * Hkv * ((Skv + 127) / 128);
+  if (items >= 256) return 0;
+  const int g = Hq / Hkv;
+  for (int d = 2; d < g; ++d)
+    if (g % d == 0 && items * d >= 256) return d;
+  return g;
 }
 inline size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 inline size_t bwd_delta_bytes(int B, int Hq, int Sq) { return round256((size_t)B * Hq * Sq * sizeof(float)); }
-inline size_t bwd_partial_bytes(int B, int Hq, int Skv, int D) {
-  return round256((size_t)B * Skv * Hq * D * sizeof(float));
+// one fp32 partial dK (or dV) buffer [B, Skv, Hkv * parts, D]
+inline size_t bwd_partial_bytes(int B, int Hkv, int parts, int Skv, int D) {
+  return round256((size_t)B * Skv * Hkv * parts * D * sizeof(float));
 }
 
 // Counts one kernel launch issued by the library (see attn_launch_count()).
@@ -54,7 +64,7 @@ void count_launches(int n);
 cudaError_t simt_fwd(const Problem& p, cudaStream_t stream);
 cudaError_t simt_bwd(const Problem& p, cudaStream_t stream);
 // delta = rowsum(dO * O) into p.delta (one warp per row), for the CUDA-core backward
-// (the bf16 backward forms delta inside its dQ kernel).
+// (the bf16 backward has a delta kernel of its own).
 cudaError_t simt_delta(const Problem& p, cudaStream_t stream);
 
 // Tensor-core (tcgen05) kernels for bf16, sm_103a.

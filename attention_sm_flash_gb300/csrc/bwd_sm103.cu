@@ -17,9 +17,10 @@
 // dK/dV: a CTA owns 128 keys of one (batch, kv head) and loops over the query heads of
 //   the GQA group and their query tiles of 128 rows in a fixed order, so the group sum of
 //   row T15 (in-group deterministic sum) happens inside its TMEM accumulators. When such
-//   items are too few to fill the GPU (few kv heads, causal imbalance), each query head
-//   is its own item writing fp32 partial dK/dV, and a reduction kernel sums each group
-//   in head order - still deterministic, still no atomics. Keys sit on the TMEM lanes:
+//   items are too few to fill the GPU (few kv heads, causal imbalance), the group's
+//   query heads are split into a few runs of consecutive heads, each its own item writing
+//   fp32 partial dK/dV, and a reduction kernel sums each group's partials in head order -
+//   still deterministic, still no atomics. Keys sit on the TMEM lanes:
 //   S^T = K Q^T and dP^T = V dO^T; the elementwise warps write P^T and dS^T (bf16) over
 //   the first columns of each, and dV += P^T dO, dK += dS^T Q take A from TMEM. The MMAs
 //   of one tile are issued S^T, dP^T, dV, dK, so that each wait of the issuing threads
@@ -72,12 +73,14 @@ struct BwdParams {
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  float* part_dk;  // split mode: fp32 per-query-head partial dK, dV [B, Skv, Hq, D]
+  // split mode: fp32 partial dK, dV [B, Skv, Hkv * split, D]; slot kvh * split + r holds
+  // the sum over query heads kvh * g + r * g / split .. + g / split - 1 (g = Hq / Hkv)
+  float* part_dk;
   float* part_dv;
   const int32_t* kv_lens;
   unsigned int* err;
   int B, Hq, Hkv, Sq, Skv, causal;
-  int split;
+  int split;  // parts per GQA group (0: not split)
   int n_items;
   float scale, scale_log2;
   uint64_t timeout_ns;
@@ -546,14 +549,15 @@ struct DkvCtl {
 
 struct DkvItem {
   int b, kvh, j0, L;
-  int h0, heads;  // query heads h0 .. h0 + heads - 1 (the whole group, or one in split mode)
+  int h0, heads;  // query heads h0 .. h0 + heads - 1 (the whole group, or a run of it)
+  int slot;       // split mode: the partial dK/dV slot, kvh * split + r
   int i_start, per_head, n_tiles;
 };
 
 __device__ __forceinline__ DkvItem dkv_decode(int idx, const BwdParams& p) {
   const int n_kt = (p.Skv + kT - 1) / kT;
   const int g = p.Hq / p.Hkv;
-  const int gs = p.split ? g : 1;  // items per (batch, kv head, key tile)
+  const int gs = p.split ? p.split : 1;  // items per (batch, kv head, key tile)
   const int BK = p.B * p.Hkv;
   int b, kvh, kt, r;
   if (p.causal) {
@@ -577,8 +581,9 @@ __device__ __forceinline__ DkvItem dkv_decode(int idx, const BwdParams& p) {
   it.kvh = kvh;
   it.j0 = kt * kT;
   it.L = kv_len_of(p, b, kvh);
-  it.h0 = kvh * g + r;
-  it.heads = p.split ? 1 : g;
+  it.heads = g / gs;
+  it.h0 = kvh * g + r * it.heads;
+  it.slot = kvh * gs + r;
   const int n_qt = (p.Sq + kT - 1) / kT;
   it.i_start = 0;
   it.per_head = 0;
@@ -800,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
       const int j = it.j0 + r;
       const bool key_ok = j < it.L;
       const int64_t orow = ((static_cast<int64_t>(it.b) * p.Skv + j) * p.Hkv + it.kvh) * D;
-      const int64_t prow = ((static_cast<int64_t>(it.b) * p.Skv + j) * p.Hq + it.h0) * D;
+      const int64_t prow = ((static_cast<int64_t>(it.b) * p.Skv + j) * p.Hkv * p.split + it.slot) * D;
       if (it.n_tiles == 0) {
         if (j < p.Skv) {
           if (p.split) {
@@ -907,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         tmem_ld32(tacc + cc * 32, v);
         if (j < p.Skv) {
           if (p.split) {
-            // this query head's share, unscaled; the group reduction scales dK
+            // this run of query heads' share, unscaled; the group reduction scales dK
             float4* d4 = reinterpret_cast<float4*>(pdst + cc * 32);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -966,25 +971,22 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
 }
 
 // ===================================================================== group reduction
-// Split mode: dK[b, j, kvh] = scale * sum over the group's query heads r = 0 .. g - 1 (in
-// that order) of the partial dK[b, j, kvh * g + r]; likewise dV (unscaled). Each thread
-// reduces 4 consecutive elements of one (b, j, kvh) row.
+// Split mode: dK[b, j, kvh] = scale * sum over the group's parts r = 0 .. parts - 1 (in
+// that order) of the partial dK[b, j, kvh * parts + r]; likewise dV (unscaled). Each
+// thread reduces 4 consecutive elements of one (b, j, kvh) row.
 __global__ void __launch_bounds__(256) bwd_group_reduce_kernel(const float* __restrict__ part_dk,
                                                                const float* __restrict__ part_dv,
                                                                __nv_bfloat16* dk, __nv_bfloat16* dv,
-                                                               int B, int Skv, int Hq, int Hkv, int D,
+                                                               int B, int Skv, int Hkv, int parts, int D,
                                                                float scale) {
-  const int g = Hq / Hkv;
   const int64_t n4 = (int64_t)B * Skv * Hkv * D / 4;
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= n4) return;
   const int d4 = (int)(e % (D / 4));
   const int64_t row = e / (D / 4);  // (b * Skv + j) * Hkv + kvh
-  const int kvh = (int)(row % Hkv);
-  const int64_t bj = row / Hkv;
-  const int64_t src0 = (bj * Hq + (int64_t)kvh * g) * D + 4 * d4;
+  const int64_t src0 = row * parts * D + 4 * d4;
   float4 sk = make_float4(0.f, 0.f, 0.f, 0.f), sv = sk;
-  for (int r = 0; r < g; ++r) {
+  for (int r = 0; r < parts; ++r) {
     const float4 a = __ldg(reinterpret_cast<const float4*>(part_dk + src0 + (int64_t)r * D));
     const float4 c = __ldg(reinterpret_cast<const float4*>(part_dv + src0 + (int64_t)r * D));
     sk.x += a.x; sk.y += a.y; sk.z += a.z; sk.w += a.w;
@@ -1092,7 +1094,7 @@ cudaError_t launch_bwd(const Problem& p, int dev, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   if (p.Skv > 0) {
-    prm.n_items = p.B * p.Hkv * ((p.Skv + kT - 1) / kT) * (p.split ? p.Hq / p.Hkv : 1);
+    prm.n_items = p.B * p.Hkv * ((p.Skv + kT - 1) / kT) * (p.split ? p.split : 1);
     constexpr size_t smem = dkdv_smem<D, NST>();
     cudaError_t e = set_smem(bwd_dkdv_sm103_kernel<D, NST>, smem, dev, D == 64 ? 0 : 1);
     if (e != cudaSuccess) return e;
@@ -1117,7 +1119,7 @@ cudaError_t launch_bwd(const Problem& p, int dev, cudaStream_t s) {
     if (p.split) {
       const int64_t n4 = (int64_t)p.B * p.Skv * p.Hkv * D / 4;
       bwd_group_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
-          p.part_dk, p.part_dv, prm.dk, prm.dv, p.B, p.Skv, p.Hq, p.Hkv, D, p.scale);
+          p.part_dk, p.part_dv, prm.dk, prm.dv, p.B, p.Skv, p.Hkv, p.split, D, p.scale);
       count_launches(1);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;

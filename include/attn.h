@@ -101,7 +101,7 @@ ATTN_API attn_status_t attn_fwd(const void* q, const void* k, const void* v, voi
  * attn_bwd_workspace_size(...) bytes of device memory, 256-byte aligned, for the call's
  * exclusive use until the stream reaches the end of the call (ATTN_ERR_WORKSPACE
  * otherwise). The workspace holds delta = rowsum(dO * O) [B, Hq, Sq] fp32 and, when
- * attn_bwd_workspace_size() says so, fp32 partial dK/dV of each query head.
+ * attn_bwd_workspace_size() says so, fp32 partial dK/dV of runs of query heads.
  */
 ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
@@ -110,9 +110,11 @@ ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, con
                        void* workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /* Bytes of device workspace attn_bwd needs for these sizes (0 for an empty problem):
- * delta [B, Hq, Sq] fp32, plus, for bf16 GQA problems with few (batch, kv head, key
- * tile) work items, fp32 per-query-head partial dK and dV [B, Skv, Hq, D] that a
- * second kernel sums over each group in a fixed order. A pure function of the sizes. */
+ * delta [B, Hq, Sq] fp32, plus, for bf16 GQA problems with fewer than 256 (batch, kv
+ * head, 128-key tile) work items, fp32 partial dK and dV [B, Skv, Hkv * P, D] that a
+ * second kernel sums over each group in a fixed order. P, the number of parts each
+ * group of G = Hq / Hkv query heads is split into, is the smallest divisor of G above 1
+ * that brings the items to 256 or more, else G. A pure function of the sizes. */
 ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int D,
                                         attn_dtype_t dtype);
 

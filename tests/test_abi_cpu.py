@@ -42,9 +42,17 @@ def test_workspace_size(lib):
     # MHA: delta only
     n = attn.attn_bwd_workspace_size(8, 12, 12, 1024, 1024, 64, attn.ATTN_BF16)
     assert n == 8 * 12 * 1024 * 4
-    # GQA with few (batch, kv head, key tile) items: delta + fp32 partial dK, dV per head
+    # GQA with few (batch, kv head, key tile) items: delta + fp32 partial dK, dV of P
+    # parts per group. 4 x 2 x 16 = 128 items: P = 2 (the smallest divisor of the group
+    # size 4 giving >= 256 items)
     n = attn.attn_bwd_workspace_size(4, 8, 2, 2048, 2048, 128, attn.ATTN_BF16)
-    assert n == 4 * 8 * 2048 * 4 + 2 * 4 * 2048 * 8 * 128 * 4 and n % 256 == 0
+    assert n == 4 * 8 * 2048 * 4 + 2 * 4 * 2048 * (2 * 2) * 128 * 4 and n % 256 == 0
+    # 1 x 1 x 3 items, group of 4: no divisor reaches 256, one part per query head
+    n = attn.attn_bwd_workspace_size(1, 4, 1, 257, 257, 128, attn.ATTN_BF16)
+    assert n == 256 * (-(-(4 * 257 * 4) // 256)) + 2 * 256 * (-(-(257 * 4 * 128 * 4) // 256))
+    # 1 x 1 x 65 items, group of 8: P = 4 (65 x 2 < 256 <= 65 x 4)
+    n = attn.attn_bwd_workspace_size(1, 8, 1, 130, 8200, 64, attn.ATTN_BF16)
+    assert n == 256 * (-(-(8 * 130 * 4) // 256)) + 2 * 256 * (-(-(8200 * 4 * 64 * 4) // 256))
     # many items, or fp32: delta only
     assert attn.attn_bwd_workspace_size(64, 8, 2, 2048, 2048, 128, attn.ATTN_BF16) == 64 * 8 * 2048 * 4
     assert attn.attn_bwd_workspace_size(4, 8, 2, 2048, 2048, 128, attn.ATTN_F32) == 4 * 8 * 2048 * 4

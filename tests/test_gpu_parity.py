@@ -24,6 +24,9 @@ SMALL = [
     ("s_bf16_d64_causal_tall", 1, 2, 2, 390, 130, 64, "bf16", True, "none", 0, 0),
     ("s_f32_d64_causal_tall", 1, 2, 2, 400, 130, 64, "f32", True, "none", 0, 0),
     ("s_f32_d128_varlen", 2, 4, 2, 161, 290, 128, "f32", False, "per_head_uniform", 0, 290),
+    # 65 key tiles of one kv head and a group of 8: the dK/dV work splits into 4 runs of
+    # 2 query heads each, summed by the group reduction
+    ("s_bf16_d64_gqa8_longkv", 1, 8, 1, 130, 8200, 64, "bf16", False, "none", 0, 0),
 ]
 
 
