@@ -912,13 +912,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         tmem_ld32(tacc + cc * 32, v);
         if (j < p.Skv) {
           if (p.split) {
-            // this run of query heads' share, unscaled; the group reduction scales dK
-            float4* d4 = reinterpret_cast<float4*>(pdst + cc * 32);
+            // this run of query heads' share, unscaled (the group reduction scales dK), in
+            // 32-byte stores: the workspace rows are 256-byte aligned
+            if (!key_ok) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              d4[e] = key_ok ? make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                           __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]))
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int e = 0; e < 32; ++e) v[e] = 0u;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) st_global_v8(pdst + cc * 32 + 8 * e, v + 8 * e);
           } else if (key_ok) {
             store_row_bf16(dst + cc * 32, v, mul);
           } else {

@@ -143,6 +143,13 @@ __device__ __forceinline__ void tma_store_wait_read() {
 // until this thread's committed stores are complete
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// One 32-byte global store of 8 words (dst 32-byte aligned)
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Programmatic dependent launch: from this point the next kernel of the stream, when it
 // was launched as a programmatic dependent, may be scheduled on SMs this grid frees
 __device__ __forceinline__ void griddep_launch_dependents() {
