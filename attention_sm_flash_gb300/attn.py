@@ -27,6 +27,7 @@ ATTN_ERR_TIMEOUT = -4
 ATTN_ERR_WORKSPACE = -5
 ATTN_DEVERR_KVLEN = 0x1
 ATTN_DEVERR_TIMEOUT = 0x2
+ATTN_DEVERR_LAYOUT = 0x4
 
 EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_peek_device_error",
             "attn_status_string", "attn_build_info", "attn_launch_count", "attn_bwd_noalloc",

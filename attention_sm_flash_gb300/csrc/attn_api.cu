@@ -165,6 +165,7 @@ extern "C" attn_status_t attn_peek_device_error(uint32_t* bits, attn_stream_t st
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   if (bits != nullptr) *bits = word;
   if (word & ATTN_DEVERR_TIMEOUT) return ATTN_ERR_TIMEOUT;
+  if (word & ATTN_DEVERR_LAYOUT) return ATTN_ERR_CUDA;
   if (word & ATTN_DEVERR_KVLEN) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }

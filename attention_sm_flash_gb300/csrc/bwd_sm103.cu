@@ -60,6 +60,7 @@ constexpr int kThreads = 384;  // warp 0 producer, warps 1 and 10 MMA issuers, w
 constexpr int kAccWarp = 10;
 constexpr int kStatWarp = 11;   // dQ kernel: stages per-row LSE and delta, one item ahead
 constexpr int kEwThreads = 256;
+constexpr int kEwWarps = kEwThreads / 32;  // the count of barriers the elementwise warps arrive on
 constexpr int kT = 128;        // rows of every tile: keys and queries alike
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kTeardownNs = 200000000ull;
@@ -219,18 +220,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_sm103_kernel(const __grid_
       mbar_init(&c.v_empty[s], 1);
     }
     mbar_init(&c.s_full, 1);
-    mbar_init(&c.s_free, kEwThreads);
+    mbar_init(&c.s_free, kEwWarps);
     for (int u = 0; u < 2; ++u) {
       mbar_init(&c.dp_full[u], 1);
-      mbar_init(&c.ds_ready[u], kEwThreads);
+      mbar_init(&c.ds_ready[u], kEwWarps);
       mbar_init(&c.dq_done[u], 1);
     }
     mbar_init(&c.acc_done, 1);
-    mbar_init(&c.acc_free, kEwThreads);
+    mbar_init(&c.acc_free, kEwWarps);
     mbar_init(&c.mma_final, 1);
     mbar_init(&c.mma_final2, 1);
     mbar_init(&c.dl_full, 1);
-    mbar_init(&c.dl_free, kEwThreads);
+    mbar_init(&c.dl_free, kEwWarps);
     c.abort = 0;
     fence_mbar_init();
   }
@@ -451,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_sm103_kernel(const __grid_
       // and a row past the end get P = 0
       if (!wait_phase_warp(&c.dl_full, dcnt & 1, wc)) { ok = false; break; }
       const float dl = c.delta[r], nl2 = c.nlse[r];
-      mbar_arrive(&c.dl_free);
+      mbar_arrive_warp(&c.dl_free);
       ++dcnt;
       const float2 nl2v = make_float2(nl2, nl2), ndl = make_float2(-dl, -dl);
       // keys j < kend are visible to this row
@@ -463,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_sm103_kernel(const __grid_
         float pr[64];
         tmem_ld64(t_s + lane_off + 64 * hsel, reinterpret_cast<uint32_t*>(pr));
         tc_fence_before();
-        mbar_arrive(&c.s_free);
+        mbar_arrive_warp(&c.s_free);
         const int limit = kend - jt * kT - 64 * hsel;
         // every key of this half visible to every row of the warp: no masking
         const bool full = __all_sync(0xffffffffu, limit >= 64);
@@ -508,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_sm103_kernel(const __grid_
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&c.ds_ready[u]);
+        mbar_arrive_warp(&c.ds_ready[u]);
       }
       if (!ok) break;
       if (!wait_phase_warp(&c.acc_done, item_cnt & 1, wc)) { ok = false; break; }
@@ -520,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_sm103_kernel(const __grid_
         if (row_ok) store_row_bf16(dst + cc * 32, v, p.scale);
       }
       tc_fence_before();
-      mbar_arrive(&c.acc_free);
+      mbar_arrive_warp(&c.acc_free);
       ++item_cnt;
     }
   }
@@ -537,8 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_sm103_kernel(const __grid_
 template <int NST>
 struct DkvCtl {
   uint64_t k_full, k_empty, v_full, v_empty;
-  uint64_t st_full[NST], st_empty[NST];
-  uint64_t s_full, dp_full, p_ready, ds_ready, dv_done, dk_done;
+  // a stage's Q and dO are released separately: dO once dP^T and dV have read it (two
+  // commits, one per issuer), Q once dK has, later in the tile
+  uint64_t q_full[NST], q_empty[NST], do_full[NST], do_empty[NST];
+  uint64_t s_full, s_free, dp_full, p_ready, ds_ready, dv_done, dk_done;
   uint64_t acc_done, acc_free, mma_final, mma_final2;
   uint32_t tmem_base;
   int abort;
@@ -604,14 +607,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
   constexpr uint32_t kIdescSP = idesc_bf16_f32(kT, kT, false, false);
   constexpr uint32_t kIdescAcc = idesc_bf16_f32(kT, D, false, true);
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  // no alignment slack: every byte of the 227 KB is used, and the dynamic shared memory
+  // of a kernel without static shared memory starts 1024-byte aligned (checked: the
+  // 128-byte swizzle of the tiles needs it)
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if ((smem_u32(smem) & 1023u) != 0u) {
+    if (threadIdx.x == 0) atomicOr(p.err, ATTN_DEVERR_LAYOUT);
+    return;
+  }
   uint8_t* sK = smem;
   uint8_t* sV = smem + kTile;
   uint8_t* sQ = smem + 2 * kTile;                 // NST stages
   uint8_t* sdO = smem + 2 * kTile + NST * kTile;  // NST stages
-  DkvCtl<NST>& c = *reinterpret_cast<DkvCtl<NST>*>(smem + 2 * kTile + 2 * NST * kTile);
+  uint8_t* sP = smem + 2 * kTile + 2 * NST * kTile;  // P^T (bf16, keys x queries, K-major)
+  DkvCtl<NST>& c = *reinterpret_cast<DkvCtl<NST>*>(sP + kT * kT * 2);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -621,17 +630,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
     mbar_init(&c.v_full, 1);
     mbar_init(&c.v_empty, 1);
     for (int s = 0; s < NST; ++s) {
-      mbar_init(&c.st_full[s], 2);  // TMA (expect_tx) + LSE/delta stores
-      mbar_init(&c.st_empty[s], 1);
+      mbar_init(&c.q_full[s], 2);  // TMA (expect_tx) + LSE/delta stores
+      mbar_init(&c.q_empty[s], 1);
+      mbar_init(&c.do_full[s], 1);
+      mbar_init(&c.do_empty[s], 2);
     }
     mbar_init(&c.s_full, 1);
+    mbar_init(&c.s_free, kEwWarps);
     mbar_init(&c.dp_full, 1);
-    mbar_init(&c.p_ready, kEwThreads);
-    mbar_init(&c.ds_ready, kEwThreads);
+    mbar_init(&c.p_ready, kEwWarps);
+    mbar_init(&c.ds_ready, kEwWarps);
     mbar_init(&c.dv_done, 1);
     mbar_init(&c.dk_done, 1);
     mbar_init(&c.acc_done, 1);
-    mbar_init(&c.acc_free, kEwThreads);
+    mbar_init(&c.acc_free, kEwWarps);
     mbar_init(&c.mma_final, 1);
     mbar_init(&c.mma_final2, 1);
     c.abort = 0;
@@ -644,7 +656,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // TMEM columns: S^T [0, 128), dP^T [128, 256), dV [256, 256 + D), dK [256 + D, 256 + 2 D)
+  // TMEM columns: S^T [0, 128), dP^T [128, 256), dV [256, 256 + D), dK [256 + D, 256 + 2 D).
+  // P^T goes to shared memory (dV += P^T dO reads both operands there), so S^T(g + 1) may
+  // be issued as soon as the elementwise warps hold S^T(g) in registers.
   const uint32_t tmem = c.tmem_base;
   const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + D;
   WaitCtl wc{&c.abort, p.err, p.timeout_ns};
@@ -671,11 +685,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
       for (int t = 0; t < it.n_tiles; ++t) {
         const int h = it.h0 + t / it.per_head;
         const int i0 = (it.i_start + t % it.per_head) * kT;
-        if (!wait_phase_warp(&c.st_empty[st], st_par ^ 1, wc)) { ok = false; break; }
+        // dO first: its stage slot is released earlier in the tile than Q's
+        if (!wait_phase_warp(&c.do_empty[st], st_par ^ 1, wc)) { ok = false; break; }
         if (lane == 0) {
-          mbar_expect_tx(&c.st_full[st], 2 * kTile);
-          load_tile<D>(sQ + st * kTile, &p.tm_q, &c.st_full[st], h, i0, it.b, kT);
-          load_tile<D>(sdO + st * kTile, &p.tm_do, &c.st_full[st], h, i0, it.b, kT);
+          mbar_expect_tx(&c.do_full[st], kTile);
+          load_tile<D>(sdO + st * kTile, &p.tm_do, &c.do_full[st], h, i0, it.b, kT);
+        }
+        if (!wait_phase_warp(&c.q_empty[st], st_par ^ 1, wc)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_expect_tx(&c.q_full[st], kTile);
+          load_tile<D>(sQ + st * kTile, &p.tm_q, &c.q_full[st], h, i0, it.b, kT);
         }
         issued |= 1u << st;
         last_par = (last_par & ~(1u << st)) | (st_par << st);
@@ -695,18 +714,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
           c.ndel[st][q] = nd;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&c.st_full[st]);
+        if (lane == 0) mbar_arrive(&c.q_full[st]);
         if (++st == NST) { st = 0; st_par ^= 1; }
       }
     }
     for (int s = 0; s < NST; ++s)
-      if (issued & (1u << s)) wait_phase_teardown(&c.st_full[s], (last_par >> s) & 1, kTeardownNs);
+      if (issued & (1u << s)) {
+        wait_phase_teardown(&c.q_full[s], (last_par >> s) & 1, kTeardownNs);
+        wait_phase_teardown(&c.do_full[s], (last_par >> s) & 1, kTeardownNs);
+      }
     if (k_cnt > 0) wait_phase_teardown(&c.k_full, (k_cnt - 1) & 1, kTeardownNs);
     if (v_cnt > 0) wait_phase_teardown(&c.v_full, (v_cnt - 1) & 1, kTeardownNs);
   } else if (warp == 1) {
     // --------------------------------------------------- MMA issuer: S^T and dP^T
-    // S^T(g) waits until dV(g - 1) has read P^T(g - 1) from the same columns, dP^T(g)
-    // until dK(g - 1) has read dS^T(g - 1)
+    // S^T(g) waits until the elementwise warps have loaded S^T(g - 1), dP^T(g) until
+    // dK(g - 1) has read dS^T(g - 1) from the same columns
     if (lane == 0) {
       const uint32_t sKa = smem_u32(sK), sVa = smem_u32(sV);
       const uint32_t sQa = smem_u32(sQ), sdOa = smem_u32(sdO);
@@ -716,9 +738,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         const DkvItem it = dkv_decode(idx, p);
         if (it.n_tiles == 0) continue;
         for (int t = 0; t < it.n_tiles; ++t) {
-          if (!wait_phase(&c.st_full[st], st_par, wc)) { ok = false; break; }
+          if (!wait_phase(&c.q_full[st], st_par, wc)) { ok = false; break; }
           if (t == 0 && !wait_phase(&c.k_full, kv_cnt & 1, wc)) { ok = false; break; }
-          if (gt >= 1 && !wait_phase(&c.dv_done, (gt - 1) & 1, wc)) { ok = false; break; }
+          if (gt >= 1 && !wait_phase(&c.s_free, (gt - 1) & 1, wc)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -729,6 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
           mma_commit(&c.s_full);
           if (t == it.n_tiles - 1) mma_commit(&c.k_empty);
           if (t == 0 && !wait_phase(&c.v_full, kv_cnt & 1, wc)) { ok = false; break; }
+          if (!wait_phase(&c.do_full[st], st_par, wc)) { ok = false; break; }
           if (gt >= 1 && !wait_phase(&c.dk_done, (gt - 1) & 1, wc)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -738,6 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
                    kIdescSP, kk > 0 ? 1u : 0u);
           }
           mma_commit(&c.dp_full);
+          mma_commit(&c.do_empty[st]);
           if (t == it.n_tiles - 1) mma_commit(&c.v_empty);
           if (++st == NST) { st = 0; st_par ^= 1; }
           ++gt;
@@ -750,26 +774,29 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
     __syncwarp();
   } else if (warp == kAccWarp) {
     // ------------------------------------- MMA issuer: dV += P^T dO, dK += dS^T Q
-    // P^T(g) / dS^T(g) ready imply S^T(g) / dP^T(g) complete, so the commit to the Q/dO
-    // stage's empty barrier also covers the other issuer's reads of Q(g) and dO(g)
+    // dS^T(g) ready implies S^T(g) and dP^T(g) complete, so the commit to Q's empty
+    // barrier after dK(g) also covers the other issuer's read of Q(g); dO's empty barrier
+    // takes a commit from each issuer, since dP^T(g) may still run when dV(g) is issued
     if (lane == 0) {
-      const uint32_t sQa = smem_u32(sQ), sdOa = smem_u32(sdO);
+      const uint32_t sQa = smem_u32(sQ), sdOa = smem_u32(sdO), sPa = smem_u32(sP);
       uint32_t st = 0, gt = 0, item_cnt = 0;
       bool ok = true;
       for (int ps = 0, idx = item_at(0); ok && idx < p.n_items; idx = item_at(++ps)) {
         const DkvItem it = dkv_decode(idx, p);
         if (it.n_tiles == 0) continue;
         for (int t = 0; t < it.n_tiles; ++t) {
-          // dV += P^T dO (P^T of queries 64 h .. 64 h + 63 sits in columns 64 h .. 64 h + 31)
+          // dV += P^T dO, both operands in shared memory
           if (!wait_phase(&c.p_ready, gt & 1, wc)) { ok = false; break; }
           if (t == 0 && !wait_phase(&c.acc_free, (item_cnt & 1) ^ 1, wc)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk) {
+            const uint32_t off = (kk / 4) * kChunk + (kk % 4) * 32;
             const uint64_t bdo = smem_desc_sw128(sdOa + st * kTile + kk * 16 * 128, kChunk, 1024);
-            mma_ts(t_dv, t_s + (kk / 4) * 64 + (kk % 4) * 8, bdo, kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
+            mma_ss(t_dv, smem_desc_sw128(sPa + off, 16, 1024), bdo, kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&c.dv_done);
+          mma_commit(&c.do_empty[st]);
           // dK += dS^T Q
           if (!wait_phase(&c.ds_ready, gt & 1, wc)) { ok = false; break; }
           tc_fence_after();
@@ -779,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
             mma_ts(t_dk, t_dp + (kk / 4) * 64 + (kk % 4) * 8, bq, kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&c.dk_done);
-          mma_commit(&c.st_empty[st]);
+          mma_commit(&c.q_empty[st]);
           if (++st == NST) st = 0;
           ++gt;
         }
@@ -819,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
       }
       for (int t = 0; t < it.n_tiles; ++t, ++gt) {
         const uint32_t s = gt % NST;
-        if (!wait_phase_warp(&c.st_full[s], (gt / NST) & 1, wc)) { ok = false; break; }
+        if (!wait_phase_warp(&c.q_full[s], (gt / NST) & 1, wc)) { ok = false; break; }
         // the tile's per-column -LSE go to registers before the wait for S^T: while SS MMAs
         // run they take the whole shared-memory bandwidth, and a load issued on the
         // critical path costs several hundred cycles
@@ -836,6 +863,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         const uint32_t ts = t_s + lane_off + 64 * hsel;
         float pr[64];
         tmem_ld64(ts, reinterpret_cast<uint32_t*>(pr));
+        tc_fence_before();
+        mbar_arrive_warp(&c.s_free);  // S^T(g)'s columns may take S^T(g + 1)
         // every query of this half visible to every key of the warp: no masking
         if (__all_sync(0xffffffffu, key_ok && qlo <= 0)) {
 #pragma unroll
@@ -856,10 +885,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(pr[2 * e], pr[2 * e + 1]);
-        tmem_st32(ts, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&c.p_ready);
+        // P^T(g) into the shared tile once dV(g - 1) has read P^T(g - 1) there: row r of
+        // the 64-query chunk hsel, 16-byte unit u (queries 8 u .. 8 u + 7) at the
+        // 128-byte-swizzled position u ^ (r mod 8)
+        if (gt >= 1 && !wait_phase_warp(&c.dv_done, (gt - 1) & 1, wc)) { ok = false; break; }
+        {
+          uint8_t* prow = sP + hsel * kChunk + r * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(prow + ((u ^ (r & 7)) * 16)) =
+                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive_warp(&c.p_ready);
         // dS^T = P^T * (dP^T - delta), over dP^T's first columns of this half; a key past
         // the valid length may turn NaN here, but its dK row is written as zeros. The
         // -delta of each 32-column half is fetched ahead of its use, as above.
@@ -895,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&c.ds_ready);
+        mbar_arrive_warp(&c.ds_ready);
       }
       if (!ok) break;
       // epilogue: half 0 writes dV, half 1 writes dK (times the scale); rows past the
@@ -928,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         }
       }
       tc_fence_before();
-      mbar_arrive(&c.acc_free);
+      mbar_arrive_warp(&c.acc_free);
       ++item_cnt;
     }
   }
@@ -1002,15 +1040,15 @@ __global__ void __launch_bounds__(256) bwd_group_reduce_kernel(const float* __re
 // ============================================================================ host side
 template <int D, int NST>
 constexpr size_t dkdv_smem() {
-  return 1024 + 2 * (size_t)kT * D * 2 + 2 * (size_t)NST * kT * D * 2 + sizeof(DkvCtl<NST>);
+  return 2 * (size_t)kT * D * 2 + 2 * (size_t)NST * kT * D * 2 + (size_t)kT * kT * 2 + sizeof(DkvCtl<NST>);
 }
 template <int D, int NK, int NV>
 constexpr size_t dq_smem() {
   return 1024 + (size_t)(2 + NK + NV) * kT * D * 2 + sizeof(DqCtl<NK, NV>);
 }
-// dK/dV: Q/dO stages of 128 queries, as many as fit in 227 KB next to K and V
+// dK/dV: Q/dO stages of 128 queries, as many as fit in 227 KB next to K, V and P^T
 template <int D>
-constexpr int kStages = D == 64 ? 5 : 2;
+constexpr int kStages = D == 64 ? 4 : 2;
 static_assert(dkdv_smem<64, kStages<64>>() <= 232448 && dkdv_smem<128, kStages<128>>() <= 232448,
               "dK/dV shared memory");
 // dQ: K and V rings

@@ -25,6 +25,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
+// One arrival per warp, on a barrier that counts warps: __syncwarp orders every lane's
+// prior accesses (shared memory; TMEM after the lane's tcgen05 wait and fence) before
+// lane 0's release-arrive. A single arrive is far cheaper than 32 while MMAs keep the
+// shared-memory pipe busy.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
                    smem_u32(bar)),

@@ -81,6 +81,9 @@ typedef enum {
 /* Bits of the device error word. */
 #define ATTN_DEVERR_KVLEN 0x1u   /* a kv_lens entry was outside [0, Skv]; it was clamped */
 #define ATTN_DEVERR_TIMEOUT 0x2u /* a bounded barrier wait ran out; outputs are invalid */
+#define ATTN_DEVERR_LAYOUT 0x4u  /* a kernel's shared memory was not 1024-byte aligned, which
+                                    its swizzled tiles need; it computed nothing, outputs are
+                                    invalid */
 
 /*
  * Forward. q, k, v: inputs; o: output [B, Sq, Hq, D]; lse: output [B, Hq, Sq] fp32.
@@ -158,8 +161,9 @@ ATTN_API attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void
 /*
  * Waits for `stream`, then reads and clears the current device's error word.
  * Writes the raw ATTN_DEVERR_* bits to *bits when bits is not NULL. Returns
- * ATTN_ERR_TIMEOUT if the timeout bit was set, ATTN_ERR_INVALID_ARG if only the
- * kv_lens bit was set, ATTN_OK if the word was clear, ATTN_ERR_CUDA on a CUDA error.
+ * ATTN_ERR_TIMEOUT if the timeout bit was set, else ATTN_ERR_CUDA if the layout bit was
+ * set, ATTN_ERR_INVALID_ARG if only the kv_lens bit was set, ATTN_OK if the word was
+ * clear, ATTN_ERR_CUDA on a CUDA error.
  */
 ATTN_API attn_status_t attn_peek_device_error(uint32_t* bits, attn_stream_t stream);
 
