@@ -103,6 +103,17 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
   for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
 }
 
+// the same with 32-byte stores (dst 32-byte aligned): half the store instructions, and a
+// warp's store touches 32 rows either way
+__device__ __forceinline__ void store_row_bf16_v8(__nv_bfloat16* dst, const uint32_t* v, float mul) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+  st_global_v8(dst, pk);
+  st_global_v8(dst + 16, pk + 8);
+}
+
 __device__ __forceinline__ void zero_row_bf16(__nv_bfloat16* dst, int n) {
   for (int d = 0; d < n; d += 8) *reinterpret_cast<uint4*>(dst + d) = make_uint4(0u, 0u, 0u, 0u);
 }
@@ -436,6 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_sm103_kernel(const __grid_
     const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+    // dQ rows start 32-byte aligned when the tensor does (row and column offsets are
+    // multiples of 64 bytes)
+    const bool out32 = (reinterpret_cast<uintptr_t>(p.dq) & 31u) == 0u;
     uint32_t gt = 0, item_cnt = 0, dcnt = 0;
     bool ok = true;
     for (int ps = 0, idx = item_at(0); ok && idx < p.n_items; idx = item_at(++ps)) {
@@ -518,7 +532,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_sm103_kernel(const __grid_
       for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t v[32];
         tmem_ld32(t_dq + lane_off + hsel * (D / 2) + cc * 32, v);
-        if (row_ok) store_row_bf16(dst + cc * 32, v, p.scale);
+        if (row_ok) {
+          if (out32) store_row_bf16_v8(dst + cc * 32, v, p.scale);
+          else store_row_bf16(dst + cc * 32, v, p.scale);
+        }
       }
       tc_fence_before();
       mbar_arrive_warp(&c.acc_free);
@@ -825,6 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
     const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+    const bool out32 = ((reinterpret_cast<uintptr_t>(p.dk) | reinterpret_cast<uintptr_t>(p.dv)) & 31u) == 0u;
     uint32_t gt = 0, item_cnt = 0;
     bool ok = true;
     for (int ps = 0, idx = item_at(0); ok && idx < p.n_items; idx = item_at(++ps)) {
@@ -959,7 +977,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
 #pragma unroll
             for (int e = 0; e < 4; ++e) st_global_v8(pdst + cc * 32 + 8 * e, v + 8 * e);
           } else if (key_ok) {
-            store_row_bf16(dst + cc * 32, v, mul);
+            if (out32) store_row_bf16_v8(dst + cc * 32, v, mul);
+            else store_row_bf16(dst + cc * 32, v, mul);
           } else {
             zero_row_bf16(dst + cc * 32, 32);
           }

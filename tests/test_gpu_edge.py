@@ -187,3 +187,27 @@ def test_bounded_wait_runs_out_reports_timeout_and_gpu_stays_usable():
     o_ref, lse_ref = oracle.forward(inp["q"], inp["k"], inp["v"], w.scale, False)
     compare("o_after_timeout", o, o_ref, *TOL["bf16"]["o"])
     compare("lse_after_timeout", lse, lse_ref, *TOL["bf16"]["lse"])
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_gradients_at_16_byte_aligned_outputs(D):
+    """dQ, dK, dV at addresses 16-byte but not 32-byte aligned (the API's minimum) get the
+    same bits as at aligned ones (the kernels fall back from 32-byte to 16-byte stores)."""
+    w, inp = case("bf16", B=1, Hq=4, Hkv=4, Sq=300, Skv=300, D=D, causal=True)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    o, lse = attn.forward(dev["q"], dev["k"], dev["v"], causal=True, scale=w.scale)
+    ref = attn.backward(dev["q"], dev["k"], dev["v"], o, dev["do"], lse, causal=True,
+                        scale=w.scale)
+    outs = []
+    for t in (dev["q"], dev["k"], dev["v"]):
+        buf = torch.empty(t.numel() + 8, dtype=t.dtype, device="cuda")
+        view = buf[8:8 + t.numel()].view(t.shape)
+        assert view.data_ptr() % 32 == 16
+        outs.append(view)
+    attn.attn_bwd(dev["q"], dev["k"], dev["v"], o, dev["do"], lse, *outs, causal=True,
+                  scale=w.scale, kv_lens=None)
+    torch.cuda.synchronize()
+    st, bits = attn.attn_peek_device_error()
+    assert st == attn.ATTN_OK, (st, bits)
+    for name, a, b in zip(("dq", "dk", "dv"), outs, ref):
+        assert torch.equal(a, b), name
