@@ -640,6 +640,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
   DkvCtl<NST>& c = *reinterpret_cast<DkvCtl<NST>*>(sP + kT * kT * 2);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // split mode: the group reduction that follows is a programmatic dependent of this grid
+  // (it waits for this grid's completion before reading the partials), so it may be
+  // scheduled on the SMs this grid's CTAs leave
+  if (p.split) griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     mbar_init(&c.k_full, 1);
@@ -1037,6 +1041,9 @@ __global__ void __launch_bounds__(256) bwd_group_reduce_kernel(const float* __re
                                                                __nv_bfloat16* dk, __nv_bfloat16* dv,
                                                                int B, int Skv, int Hkv, int parts, int D,
                                                                float scale) {
+  // launched as a programmatic dependent of the dK/dV kernel: the partials are complete
+  // and visible after this wait
+  griddep_wait();
   const int64_t n4 = (int64_t)B * Skv * Hkv * D / 4;
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= n4) return;
@@ -1176,8 +1183,19 @@ cudaError_t launch_bwd(const Problem& p, int dev, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (p.split) {
       const int64_t n4 = (int64_t)p.B * p.Skv * p.Hkv * D / 4;
-      bwd_group_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
-          p.part_dk, p.part_dv, prm.dk, prm.dv, p.B, p.Skv, p.Hkv, p.split, D, p.scale);
+      cudaLaunchAttribute rattr[1];
+      rattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      rattr[0].val.programmaticStreamSerializationAllowed = 1;
+      cudaLaunchConfig_t rcfg{};
+      rcfg.gridDim = dim3((unsigned)((n4 + 255) / 256));
+      rcfg.blockDim = dim3(256);
+      rcfg.stream = s;
+      rcfg.attrs = rattr;
+      rcfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&rcfg, bwd_group_reduce_kernel, static_cast<const float*>(p.part_dk),
+                             static_cast<const float*>(p.part_dv), prm.dk, prm.dv, p.B, p.Skv, p.Hkv,
+                             p.split, D, p.scale);
+      if (e != cudaSuccess) return e;
       count_launches(1);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;

@@ -163,6 +163,9 @@ __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// Programmatic dependent launch: wait until the grids this one depends on have completed
+// and their memory is visible (a no-op for a kernel launched without the attribute)
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ------------------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
