@@ -24,6 +24,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -180,9 +181,8 @@ class ClockSampler:
         if not enabled:
             return
         try:
-            os.makedirs(os.path.join(HERE, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(HERE, "gpurun_out", f"clocks_rank{os.getpid()}.csv")
-            self.fh = open(self.path, "w")
+            fd, self.path = tempfile.mkstemp(prefix=f"attn_clocks_{os.getpid()}_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
@@ -202,6 +202,10 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             rows = [[p.strip() for p in line.split(",")] for line in f]
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
         rows = [r for r in rows if len(r) >= 9]
         seen = {r[0] for r in rows}
         want = self.index if self.index in seen else (seen.pop() if len(seen) == 1 else None)

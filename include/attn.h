@@ -72,7 +72,7 @@ typedef enum {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = -1, /* a null/misaligned pointer, a bad size, a non-finite scale */
-  ATTN_ERR_UNSUPPORTED = -2, /* a valid request this build does not implement (e.g. D) */
+  ATTN_ERR_UNSUPPORTED = -2, /* a valid request this library does not implement (e.g. D) */
   ATTN_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed */
   ATTN_ERR_TIMEOUT = -4,     /* a device-side bounded wait ran out (see the error word) */
   ATTN_ERR_WORKSPACE = -5    /* the backward workspace is missing or too small */
