@@ -1000,6 +1000,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // this grid may start before the dQ grid it depends on programmatically has finished;
+  // waiting for that grid before exiting makes the completion of this grid (which the
+  // caller's later work on the stream waits for) imply the completion of the dQ grid. The
+  // dQ grid is the shorter one, so the wait costs nothing in practice.
+  griddep_wait();
 }
 
 // ========================================================================== delta
