@@ -21,13 +21,13 @@
 //   query heads are split into a few runs of consecutive heads, each its own item writing
 //   fp32 partial dK/dV, and a reduction kernel sums each group's partials in head order -
 //   still deterministic, still no atomics. Keys sit on the TMEM lanes:
-//   S^T = K Q^T and dP^T = V dO^T; the elementwise warps write P^T and dS^T (bf16) over
-//   the first columns of each, and dV += P^T dO, dK += dS^T Q take A from TMEM. The MMAs
-//   of one tile are issued S^T, dP^T, dV, dK, so that each wait of the issuing threads
-//   (P^T ready, dS^T ready, S^T's columns free, dP^T's columns free) sits behind an MMA
-//   already queued. (Double-buffering 64-query S^T / dP^T tiles instead measured slower:
-//   N = 64 MMAs are shared-memory bound and the tensor pipe then runs mixed SS / TS work
-//   from two issuing threads.)
+//   S^T = K Q^T and dP^T = V dO^T. The elementwise warps read S^T into registers (which
+//   frees its columns for the next tile's S^T), write P^T (bf16) to a shared-memory tile
+//   for dV += P^T dO, and write dS^T (bf16) over the first columns of dP^T, from where
+//   dK += dS^T Q takes A. The MMAs of one tile are issued S^T, dP^T, dV, dK, so that each
+//   wait of the issuing threads (P^T ready, dS^T ready, S^T's columns free, dP^T's columns
+//   free) sits behind an MMA already queued. A Q/dO stage is released in two halves: dO
+//   once dP^T and dV have read it, Q once dK has.
 //
 // Roles (384 threads): warp 0 TMA producer; two MMA-issuing threads, one in warp 1 for the
 // products that recompute S and dP, one in warp 10 for the accumulations (dQ, or dV and
