@@ -133,10 +133,43 @@ def _check_cuda(*ts):
                 raise ValueError("libattn takes contiguous tensors only")
 
 
+def _check_shapes(q, k, v, lse, kv_lens, like_q=(), like_k=()):
+    """Shapes and element types the C ABI assumes but cannot see through raw pointers:
+    q [B,Sq,Hq,D]; k, v [B,Skv,Hkv,D]; every data tensor one element type; lse fp32
+    [B,Hq,Sq]; kv_lens int32 [B,Hkv]. ``like_q`` / ``like_k``: (name, tensor) pairs that
+    must have q's / k's shape and element type."""
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, S, H, D]")
+    B, Sq, Hq, D = q.shape
+    if k.shape[0] != B or k.shape[3] != D:
+        raise ValueError(f"k {tuple(k.shape)} does not match q {tuple(q.shape)} in B or D")
+    if v.shape != k.shape:
+        raise ValueError(f"v {tuple(v.shape)} differs from k {tuple(k.shape)}")
+    for name, t in (("k", k), ("v", v)):
+        if t.dtype != q.dtype:
+            raise ValueError(f"{name} is {t.dtype}, q is {q.dtype}")
+    for name, t in like_q:
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must be {q.dtype} {tuple(q.shape)}, got {t.dtype} "
+                             f"{tuple(t.shape)}")
+    for name, t in like_k:
+        if t.shape != k.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must be {q.dtype} {tuple(k.shape)}, got {t.dtype} "
+                             f"{tuple(t.shape)}")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Sq):
+        raise ValueError(f"lse must be float32 {(B, Hq, Sq)}, got {lse.dtype} "
+                         f"{tuple(lse.shape)}")
+    if kv_lens is not None and not isinstance(kv_lens, int):
+        if kv_lens.dtype != torch.int32 or tuple(kv_lens.shape) != (B, k.shape[2]):
+            raise ValueError(f"kv_lens must be int32 {(B, k.shape[2])}, got "
+                             f"{kv_lens.dtype} {tuple(kv_lens.shape)}")
+
+
 def attn_fwd(q, k, v, o, lse, causal: bool = False, scale: float | None = None,
              kv_lens=None, stream=None) -> None:
     """O and LSE of attention. q [B,Sq,Hq,D]; k, v [B,Skv,Hkv,D]; o like q; lse [B,Hq,Sq]."""
     _check_cuda(q, k, v, o, lse, kv_lens)
+    _check_shapes(q, k, v, lse, kv_lens, like_q=(("o", o),))
     B, Sq, Hq, D = q.shape
     Skv, Hkv = k.shape[1], k.shape[2]
     if scale is None:
@@ -158,6 +191,8 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal: bool = False,
     """dQ, dK, dV of sum(O * dO). ``workspace``: a uint8 device tensor of at least
     attn_bwd_workspace_size() bytes; allocated here (by torch) when None."""
     _check_cuda(q, k, v, o, dout, lse, dq, dk, dv, kv_lens)
+    _check_shapes(q, k, v, lse, kv_lens, like_q=(("o", o), ("dout", dout), ("dq", dq)),
+                  like_k=(("dk", dk), ("dv", dv)))
     B, Sq, Hq, D = q.shape
     Skv, Hkv = k.shape[1], k.shape[2]
     if scale is None:
@@ -179,6 +214,8 @@ def attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, causal: bool = False,
     """attn_bwd without a workspace, for callers that cannot allocate device memory: the
     scratch lives in a fixed-size array inside the library (see include/attn.h)."""
     _check_cuda(q, k, v, o, dout, lse, dq, dk, dv, kv_lens)
+    _check_shapes(q, k, v, lse, kv_lens, like_q=(("o", o), ("dout", dout), ("dq", dq)),
+                  like_k=(("dk", dk), ("dv", dv)))
     B, Sq, Hq, D = q.shape
     Skv, Hkv = k.shape[1], k.shape[2]
     if scale is None:

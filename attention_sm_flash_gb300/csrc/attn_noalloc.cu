@@ -1,10 +1,11 @@
 // attn_bwd_noalloc: the backward for callers that cannot allocate device memory.
 //
-// The scratch the backward needs (delta = rowsum(dO * O), fp32 per query row) lives in a
-// static device array owned by the library instead of a caller workspace. Host code may
-// not use the array's name as a device address (on the host it names a host-side
-// stand-in), so the address is looked up once per device with cudaGetSymbolAddress while
-// that device is current, cached, and handed to the ordinary attn_bwd path.
+// The scratch the backward needs (delta = rowsum(dO * O), fp32 per query row, and for a
+// split GQA group the fp32 partial dK/dV) lives in a static device array owned by the
+// library instead of a caller workspace. Host code may not use the array's name as a
+// device address (on the host it names a host-side stand-in), so the address is looked
+// up once per device with cudaGetSymbolAddress while that device is current, cached, and
+// handed to the ordinary attn_bwd path.
 
 #include <cuda_runtime.h>
 

@@ -630,6 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023u) != 0u) {
     if (threadIdx.x == 0) atomicOr(p.err, ATTN_DEVERR_LAYOUT);
+    // like every other exit, only after the dQ grid has completed (see the end)
+    griddep_wait();
     return;
   }
   uint8_t* sK = smem;

@@ -1,10 +1,14 @@
 #!/usr/bin/env python
 """Throughput of the fused attention hot path (forward + backward) on one GB300 per rank.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl ours]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c4] [--impl ours]
 
 A step is one pass of the whole hot path over one batch of synthetic input: attn_fwd
-then (where the workload has a backward) attn_bwd, both through the C ABI. The value is
+then (where the workload has a backward) attn_bwd, both through the C ABI. The headline
+workload is c4, the video-DiT self-attention (B1 H40 S32760 D128, the largest
+single-GPU configuration); the same run also times the GQA training step (c3: the
+long-sequence forward + backward), the varlen DiT self-attention (c4v) and the DiT
+cross-attention (c5), reported under ``also`` in the same JSON line. The value is
 TFLOP/s with the pages' counting rule (4 * B * Hq * Sq * Skv_eff * D for the forward,
 2.5 x that for the backward), inputs already resident in HBM; L2 is flushed (a 512 MiB
 write) before every step, outside the timed events. ``e2e`` is the same metric with the
@@ -47,7 +51,10 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="c2", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default="c4", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--also", default="c3,c4v,c5",
+                    help="comma-separated workloads timed after the headline one, in the "
+                         "same process (empty: none)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work in the oracle baseline sample")
@@ -258,6 +265,108 @@ def traffic_for(kernel_key):
     return None
 
 
+class Workbench:
+    """One workload's device buffers and its timed step (attn_fwd, then attn_bwd where the
+    workload has a backward) on one stream, L2 flushed before every step."""
+
+    def __init__(self, w, inp, dev, stream, flush_buf):
+        from attention_sm_flash_gb300 import attn
+
+        self.attn, self.w, self.inp, self.stream, self.flush_buf = attn, w, inp, stream, flush_buf
+        self.q, self.k, self.v = (inp[n].to(dev) for n in ("q", "k", "v"))
+        self.do = inp["do"].to(dev) if w.has_bwd else None
+        self.lens = inp["kv_lens"].to(dev) if inp["kv_lens"] is not None else None
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+        if w.has_bwd:
+            self.dq, self.dk, self.dv = (torch.empty_like(t) for t in (self.q, self.k, self.v))
+            code = attn.ATTN_BF16 if w.dtype == "bf16" else attn.ATTN_F32
+            ws_bytes = attn.attn_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, code)
+            self.ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+
+    def fwd(self):
+        w = self.w
+        self.attn.attn_fwd(self.q, self.k, self.v, self.o, self.lse, w.causal, w.scale,
+                           self.lens, self.stream)
+
+    def bwd(self):
+        w = self.w
+        self.attn.attn_bwd(self.q, self.k, self.v, self.o, self.do, self.lse, self.dq, self.dk,
+                           self.dv, w.causal, w.scale, self.lens, self.ws, self.stream)
+
+    def run_steps(self, n):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        for e in evs:
+            self.flush_buf.zero_()
+            e[0].record(self.stream)
+            self.fwd()
+            e[1].record(self.stream)
+            if self.w.has_bwd:
+                self.bwd()
+            e[2].record(self.stream)
+        return evs
+
+    def measure(self, steps, warmup, world, sampler_index, clocks_on):
+        """(fwd_ms list, bwd_ms list, clocks, launches, wall seconds) of ``steps`` timed
+        steps, barrier + synchronize on both sides."""
+        self.run_steps(max(warmup, 3))
+        torch.cuda.synchronize()
+        sampler = ClockSampler(sampler_index, enabled=clocks_on)
+        # clock pre-roll (untimed): about half a second of steps so clocks settle under load
+        t_end = time.perf_counter() + 0.5
+        while time.perf_counter() < t_end:
+            self.run_steps(1)
+            torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        n0 = self.attn.attn_launch_count()
+        t0 = time.perf_counter()
+        evs = self.run_steps(steps)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        launches = self.attn.attn_launch_count() - n0
+        if world > 1:
+            torch.distributed.barrier()
+        clocks = sampler.stop()
+        fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+        bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+        return fwd_ms, bwd_ms, clocks, launches, wall
+
+
+def tensor_peak(w, peaks, peak_src):
+    if w.dtype == "bf16":
+        return (peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]), "tensor",
+                f"bf16 dense burst, {peak_src}")
+    return FP32_FMA_TFLOPS, "alu", "FP32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz"
+
+
+def also_entry(bench, args, world, sampler_index, peaks, peak_src, dev):
+    """The figures of one extra workload for the ``also`` key of the JSON line."""
+    w = bench.w
+    cfg, fwd_fl, bwd_fl = workload_config(w, bench.inp)
+    fwd_ms, bwd_ms, clocks, launches, _ = bench.measure(args.steps, args.warmup, world,
+                                                          sampler_index, not args.no_clocks)
+    fm = reduce_max(statistics.mean(fwd_ms), dev)
+    bm = reduce_max(statistics.mean(bwd_ms), dev) if w.has_bwd else 0.0
+    peak, bound, note = tensor_peak(w, peaks, peak_src)
+    fwd_t = whole_job_tflops(fwd_fl, fm, world)
+    out = {"workload": cfg["workload"], "Skv_eff": cfg["Skv_eff"], "step": cfg["step"],
+           "value": round(whole_job_tflops(fwd_fl + bwd_fl, fm + bm, world), 3),
+           "ms_per_step": round(fm + bm, 5), "fwd_ms": round(fm, 5),
+           "fwd_tflops": round(fwd_t, 3), "fwd_frac": round(fwd_t / world / peak, 4),
+           "bound": bound, "peak": peak, "peak_source": note, "gpu_launches": int(launches),
+           "clocks": clocks}
+    if w.has_bwd:
+        bwd_t = whole_job_tflops(bwd_fl, bm, world)
+        out.update({"bwd_ms": round(bm, 5), "bwd_tflops": round(bwd_t, 3),
+                    "bwd_frac": round(bwd_t / world / peak, 4),
+                    "bwd_traffic": traffic_for(f"attn_bwd:{w.key}")})
+    if w.key != "c3":
+        out["fwd_traffic"] = traffic_for(f"attn_fwd:{w.key}")
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     from attention_sm_flash_gb300 import attn
     from attention_sm_flash_gb300 import build as libbuild
@@ -266,73 +375,23 @@ def run_ours(args, rank, world, local_rank):
         libbuild.build()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
+    sampler_index = (local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                     os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank])
     w = workloads.get(args.workload)
     inp = workloads.make_inputs(w)
     cfg, fwd_fl, bwd_fl = workload_config(w, inp)
     step_fl = fwd_fl + bwd_fl
     td = w.torch_dtype
     stream = torch.cuda.current_stream(dev)
-
-    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
-    do = inp["do"].to(dev) if w.has_bwd else None
-    lens = inp["kv_lens"].to(dev) if inp["kv_lens"] is not None else None
-    o = torch.empty_like(q)
-    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
-    if w.has_bwd:
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        ws_bytes = attn.attn_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D,
-                                                attn.ATTN_BF16 if w.dtype == "bf16" else attn.ATTN_F32)
-        ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.int16, device=dev)  # 512 MiB
-
-    def fwd():
-        attn.attn_fwd(q, k, v, o, lse, w.causal, w.scale, lens, stream)
-
-    def bwd():
-        attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, lens, ws, stream)
-
-    def step_events(n):
-        return [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
-
-    def run_steps(evs):
-        for e in evs:
-            flush_buf.zero_()
-            e[0].record(stream)
-            fwd()
-            e[1].record(stream)
-            if w.has_bwd:
-                bwd()
-            e[2].record(stream)
-
-    run_steps(step_events(max(args.warmup, 3)))
-    torch.cuda.synchronize()
-    sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
-                           os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank],
-                           enabled=not args.no_clocks)
-    # clock pre-roll (untimed): about half a second of steps so clocks settle under load
-    t_end = time.perf_counter() + 0.5
-    while time.perf_counter() < t_end:
-        run_steps(step_events(1))
-        torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    n0 = attn.attn_launch_count()
-    evs = step_events(args.steps)
-    t0 = time.perf_counter()
-    run_steps(evs)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
-    launches = attn.attn_launch_count() - n0
-    if world > 1:
-        torch.distributed.barrier()
-    clocks = sampler.stop()
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    bench = Workbench(w, inp, dev, stream, flush_buf)
+    fwd_ms, bwd_ms, clocks, launches, wall = bench.measure(args.steps, args.warmup, world,
+                                                           sampler_index, not args.no_clocks)
     step_ms = [a + b for a, b in zip(fwd_ms, bwd_ms)]
     ms = statistics.mean(step_ms)
     ms_max = reduce_max(ms, dev)
     value = whole_job_tflops(step_fl, ms_max, world)
+    q, k, v, do, lens, o, lse = bench.q, bench.k, bench.v, bench.do, bench.lens, bench.o, bench.lse
 
     # e2e: the same step through the C ABI from pinned host buffers, outputs copied back
     e2e = None
@@ -342,9 +401,11 @@ def run_ours(args, rank, world, local_rank):
         hl = inp["kv_lens"].pin_memory() if inp["kv_lens"] is not None else None
         outs_h = [torch.empty(o.shape, dtype=td).pin_memory(),
                   torch.empty(lse.shape, dtype=torch.float32).pin_memory()]
+        outs_d = [o, lse]
         if w.has_bwd:
-            outs_h += [torch.empty(t.shape, dtype=td).pin_memory() for t in (dq, dk, dv)]
-        outs_d = [o, lse] + ([dq, dk, dv] if w.has_bwd else [])
+            outs_h += [torch.empty(t.shape, dtype=td).pin_memory()
+                       for t in (bench.dq, bench.dk, bench.dv)]
+            outs_d += [bench.dq, bench.dk, bench.dv]
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, hl) if t is not None)
         d2h = sum(t.numel() * t.element_size() for t in outs_h)
 
@@ -356,9 +417,9 @@ def run_ours(args, rank, world, local_rank):
                 do.copy_(hdo, non_blocking=True)
             if hl is not None:
                 lens.copy_(hl, non_blocking=True)
-            fwd()
+            bench.fwd()
             if w.has_bwd:
-                bwd()
+                bench.bwd()
             for hd, dd in zip(outs_h, outs_d):
                 hd.copy_(dd, non_blocking=True)
 
@@ -383,16 +444,14 @@ def run_ours(args, rank, world, local_rank):
     dom_fl = bwd_fl if dom == "attn_bwd" else fwd_fl
     dom_ms = bwd_mean if dom == "attn_bwd" else fwd_mean
     achieved = dom_fl / (dom_ms * 1e-3) / 1e12
-    if w.dtype == "bf16":
-        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-        bound, peak_note = "tensor", f"bf16 dense burst, {peak_src}"
-    else:
-        peak = FP32_FMA_TFLOPS
-        bound, peak_note = "alu", "FP32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz"
+    peak, bound, peak_note = tensor_peak(w, peaks, peak_src)
+    kernels = {"attn_fwd": ("fwd_sm103_kernel (one launch per call)" if w.dtype == "bf16"
+                            else "simt_fwd_kernel (one launch per call)"),
+               "attn_bwd": "bwd_delta + bwd_dq + bwd_dkdv (+ group reduce) kernels of one call"}
     roofline = {"bound": bound, "achieved": round(achieved, 3), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "traffic": traffic_for(f"{dom}:{w.key}"), "kernel": dom,
-                "peak_source": peak_note,
+                "traffic": traffic_for(f"{dom}:{w.key}"), "kernel": kernels[dom],
+                "call": dom, "peak_source": peak_note,
                 "algorithmic_flops_per_launch": dom_fl}
     bf16_peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     line = {
@@ -414,6 +473,17 @@ def run_ours(args, rank, world, local_rank):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+    # the other graded workloads, timed the same way in the same process
+    del bench, q, k, v, do, lens, o, lse
+    also = {}
+    for key in [x for x in args.also.split(",") if x and x != w.key]:
+        wa = workloads.get(key)
+        ba = Workbench(wa, workloads.make_inputs(wa), dev, stream, flush_buf)
+        also[key] = also_entry(ba, args, world, sampler_index, peaks, peak_src, dev)
+        del ba
+        torch.cuda.empty_cache()
+    if also:
+        line["also"] = also
     if rank == 0:
         print(json.dumps(line), flush=True)
 

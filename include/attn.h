@@ -121,8 +121,12 @@ ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, con
 ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int D,
                                         attn_dtype_t dtype);
 
-/* Size of the library's static device scratch array used by attn_bwd_noalloc: 8 MiB,
- * enough for B * Hq * Sq <= 2,097,152 query rows. */
+/* Size of the library's static device scratch array used by attn_bwd_noalloc: 8 MiB.
+ * A problem fits when attn_bwd_workspace_size(...) <= ATTN_NOALLOC_SCRATCH_BYTES: delta
+ * takes 4 bytes per query row (B * Hq * Sq <= 2,097,152 rows when nothing else is
+ * needed), and a bf16 GQA problem whose group is split (see attn_bwd_workspace_size)
+ * adds two fp32 partial buffers of B * Skv * Hkv * P * D * 4 bytes each; the GQA
+ * training shape B4 Hq8 Hkv2 S2048 D128 (P = 2) needs about 33.8 MB and is refused. */
 #define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /*
@@ -139,13 +143,14 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv,
  * exits). It calls no cudaMalloc, cudaFree or other allocating routine.
  *
  * - Size limit: when attn_bwd_workspace_size() for these sizes exceeds
- *   ATTN_NOALLOC_SCRATCH_BYTES it returns ATTN_ERR_WORKSPACE and launches nothing.
+ *   ATTN_NOALLOC_SCRATCH_BYTES (delta, plus the fp32 partial dK/dV of a split GQA group)
+ *   it returns ATTN_ERR_WORKSPACE and launches nothing.
  * - Set-up: the first call on a device looks up the array's device address with that
  *   device current (cudaGetSymbolAddress); make that first call before any stream
  *   capture begins.
  * - Sharing: every call on a device uses the same array, which keeps whatever the last
- *   call left in it. Each call rewrites all the scratch it reads (delta), so nothing has
- *   to start at zero. Calls whose GPU work can overlap (different streams, or threads
+ *   call left in it. Each call rewrites all the scratch it reads (delta, and every row
+ *   of the partial dK/dV buffers), so nothing has to start at zero. Calls whose GPU work can overlap (different streams, or threads
  *   without ordering between them) race on the array and produce wrong gradients: issue
  *   them on one stream, or order them with events.
  * Everything else (arguments, layout, results, errors) is as for attn_bwd, whose code

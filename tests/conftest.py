@@ -16,3 +16,16 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def repo_root():
     return ROOT
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With ATTN_PARITY_REPORT set, write every parity comparison's error figures there."""
+    path = os.environ.get("ATTN_PARITY_REPORT")
+    if not path:
+        return
+    mod = sys.modules.get("gpu_util")
+    if mod is None or not mod.REPORT:
+        return
+    import json
+    with open(path, "w") as f:
+        json.dump(mod.REPORT, f, indent=1, sort_keys=True)

@@ -13,6 +13,20 @@ TOL = {
     "f32": {"o": (1e-5, 1e-5), "lse": (1e-5, 1e-5), "grad": (1e-5, 1e-5)},
     "bf16": {"o": (2e-2, 2e-2), "lse": (1e-3, 0.0), "grad": (2e-2, 2e-2)},
 }
+# Whole-tensor gates on O and the gradients, on top of the element-wise bound: the
+# relative L2 error ||gpu - ref|| / ||ref|| and max|gpu - ref| / max|ref|. The element-wise
+# bound alone is vacuous where |ref| is far below atol (the DiT self-attention's near-uniform
+# softmax gives |O| ~ 0.005 against atol 2e-2). The bf16 rel-L2 limit of 1e-2 is the error
+# standard of the LingBot report's attention audit against its FP64 reference (section
+# "Attention: real inputs, backends, errors and timing"); the max ratio uses the graded
+# relative tolerance. The fp32 gates take the fp32 tolerance in the same two forms.
+GATE = {
+    "f32": {"rel_l2": 1e-5, "max_ratio": 2e-5},
+    "bf16": {"rel_l2": 1e-2, "max_ratio": 2e-2},
+}
+# every comparison's figures, keyed by name (tests/conftest.py writes them to the file named
+# by ATTN_PARITY_REPORT at the end of the session, when that variable is set)
+REPORT = {}
 GUARD = 4096  # guard elements on each side of every output buffer
 SENTINEL = 12288.0  # exact in bf16 and fp32
 
@@ -37,8 +51,11 @@ def check_guard(buf, name):
     assert torch.all(lo == SENTINEL) and torch.all(hi == SENTINEL), f"{name}: guard band written"
 
 
-def compare(name, got, ref, atol, rtol, report=None):
-    """Element-wise tolerance check; -inf positions must agree exactly; no NaN allowed."""
+def compare(name, got, ref, atol, rtol, report=None, gate=None):
+    """Element-wise tolerance check; -inf positions must agree exactly; no NaN allowed.
+
+    ``gate`` (a GATE entry) adds the whole-tensor checks: rel-L2 and max|d| / max|ref|
+    over the finite entries."""
     g = got.detach().double().cpu().numpy() if hasattr(got, "detach") else np.asarray(got)
     ref = np.asarray(ref, dtype=np.float64)
     assert g.shape == ref.shape, (name, g.shape, ref.shape)
@@ -49,14 +66,25 @@ def compare(name, got, ref, atol, rtol, report=None):
     diff = np.abs(g[fin] - ref[fin])
     bound = atol + rtol * np.abs(ref[fin])
     bad = diff > bound
-    rel_l2 = float(np.linalg.norm(g[fin] - ref[fin]) / max(np.linalg.norm(ref[fin]), 1e-300))
+    ref_norm = float(np.linalg.norm(ref[fin]))
+    rel_l2 = float(np.linalg.norm(g[fin] - ref[fin]) / max(ref_norm, 1e-300))
+    ref_max = float(np.abs(ref[fin]).max()) if diff.size else 0.0
+    max_ratio = float(diff.max() / max(ref_max, 1e-300)) if diff.size else 0.0
+    fig = {"max_abs": float(diff.max()) if diff.size else 0.0, "rel_l2": rel_l2,
+           "max_ratio": max_ratio, "ref_max": ref_max}
+    REPORT[name] = fig
     if report is not None:
-        report[name] = {"max_abs": float(diff.max()) if diff.size else 0.0, "rel_l2": rel_l2}
+        report[name] = fig
     if bad.any():
         idx = np.argmax(diff - bound)
         raise AssertionError(f"{name}: {int(bad.sum())} of {bad.size} elements out of "
                              f"tolerance; worst |d|={diff[idx]:.3e} ref={ref[fin][idx]:.4e} "
                              f"bound={bound[idx]:.3e}; rel_l2={rel_l2:.3e}")
+    if gate is not None and diff.size and ref_norm > 0.0:
+        assert rel_l2 <= gate["rel_l2"], \
+            f"{name}: rel-L2 {rel_l2:.3e} above {gate['rel_l2']:.0e}"
+        assert max_ratio <= gate["max_ratio"], \
+            f"{name}: max|d|/max|ref| {max_ratio:.3e} above {gate['max_ratio']:.0e}"
     return rel_l2
 
 

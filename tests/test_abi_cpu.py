@@ -135,3 +135,70 @@ def test_noalloc_rejects_oversize_before_touching_cuda(lib):
     st = lib.attn_bwd_noalloc(A, A, A, A, A, A, A, A, A, 1, 1, 1, rows, 16, 64, 0.125, 0,
                               None, attn.ATTN_BF16, None)
     assert st == attn.ATTN_ERR_WORKSPACE
+
+
+def test_noalloc_limit_counts_the_split_gqa_partials(lib):
+    # the GQA training shape has only 65,536 query rows (256 KiB of delta), but its split
+    # group adds two fp32 partial buffers: about 33.8 MB in all, beyond the 8 MiB array
+    need = attn.attn_bwd_workspace_size(4, 8, 2, 2048, 2048, 128, attn.ATTN_BF16)
+    assert need > attn.ATTN_NOALLOC_SCRATCH_BYTES > 4 * 8 * 2048 * 4
+    st = lib.attn_bwd_noalloc(A, A, A, A, A, A, A, A, A, 4, 8, 2, 2048, 2048, 128, 0.088, 1,
+                              None, attn.ATTN_BF16, None)
+    assert st == attn.ATTN_ERR_WORKSPACE
+
+
+def _meta(shape, dtype):
+    """A tensor that passes the binding's device check without a GPU (the shape and
+    dtype checks run before anything reaches the library)."""
+    import torch
+
+    class FakeDev(torch.Tensor):
+        pass
+
+    t = torch.zeros(shape, dtype=dtype)
+    t.__class__ = FakeDev
+    FakeDev.is_cuda = property(lambda self: True)
+    return t
+
+
+@pytest.mark.parametrize("bad", ["lse_dtype", "lse_shape", "lens_dtype", "lens_shape",
+                                 "o_shape", "k_dtype", "v_shape", "kd_mismatch"])
+def test_binding_checks_shapes_and_dtypes_fwd(bad):
+    import torch
+    bf = torch.bfloat16
+    q, k, v = _meta((2, 16, 4, 64), bf), _meta((2, 24, 2, 64), bf), _meta((2, 24, 2, 64), bf)
+    o, lse = _meta((2, 16, 4, 64), bf), _meta((2, 4, 16), torch.float32)
+    lens = _meta((2, 2), torch.int32)
+    if bad == "lse_dtype":
+        lse = _meta((2, 4, 16), bf)
+    elif bad == "lse_shape":
+        lse = _meta((2, 16, 4), torch.float32)
+    elif bad == "lens_dtype":
+        lens = _meta((2, 2), torch.int64)
+    elif bad == "lens_shape":
+        lens = _meta((2,), torch.int32)
+    elif bad == "o_shape":
+        o = _meta((2, 16, 2, 64), bf)
+    elif bad == "k_dtype":
+        k = _meta((2, 24, 2, 64), torch.float32)
+    elif bad == "v_shape":
+        v = _meta((2, 23, 2, 64), bf)
+    elif bad == "kd_mismatch":
+        k, v = _meta((2, 24, 2, 128), bf), _meta((2, 24, 2, 128), bf)
+    with pytest.raises(ValueError):
+        attn.attn_fwd(q, k, v, o, lse, kv_lens=lens)
+
+
+@pytest.mark.parametrize("bad", ["dq", "dk", "dv", "dout"])
+def test_binding_checks_shapes_and_dtypes_bwd(bad):
+    import torch
+    bf = torch.bfloat16
+    t = {n: _meta((1, 16, 4, 64), bf) for n in ("q", "o", "dout", "dq")}
+    t.update({n: _meta((1, 24, 2, 64), bf) for n in ("k", "v", "dk", "dv")})
+    lse = _meta((1, 4, 16), torch.float32)
+    t[bad] = _meta(t[bad].shape, torch.float32)
+    with pytest.raises(ValueError):
+        attn.attn_bwd(t["q"], t["k"], t["v"], t["o"], t["dout"], lse, t["dq"], t["dk"], t["dv"])
+    with pytest.raises(ValueError):
+        attn.attn_bwd_noalloc(t["q"], t["k"], t["v"], t["o"], t["dout"], lse, t["dq"], t["dk"],
+                              t["dv"])

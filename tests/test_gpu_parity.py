@@ -3,7 +3,9 @@
 Small cases run the whole oracle and span several tiles with ragged tails; the five
 workloads run at full size, with the whole oracle where it finishes in seconds (c1, c2,
 c3) and on sampled query rows of every head at the video-DiT sizes (c4, c4v, c5),
-including the first rows, tile edges and the ragged last tile.
+including the first rows, tile edges and the ragged last tile. O and the gradients also
+pass the whole-tensor gates (rel-L2 and max|d| / max|ref|), which still bite where the
+outputs are far below the element-wise atol (the DiT self-attention's |O| ~ 0.005).
 """
 
 import numpy as np
@@ -12,7 +14,7 @@ import torch
 
 import oracle
 from attention_sm_flash_gb300 import workloads
-from gpu_util import TOL, compare, run_bwd, run_fwd
+from gpu_util import GATE, TOL, compare, run_bwd, run_fwd
 
 pytestmark = pytest.mark.gpu
 
@@ -38,20 +40,20 @@ def _small(c):
 
 
 def full_check(w, inp, do_bwd=True):
-    tol = TOL[w.dtype]
+    tol, gate = TOL[w.dtype], GATE[w.dtype]
     o, lse = run_fwd(inp, w)
     o_ref, lse_ref = oracle.forward(inp["q"], inp["k"], inp["v"], w.scale, w.causal,
                                     inp["kv_lens"])
-    compare("o", o, o_ref, *tol["o"])
-    compare("lse", lse, lse_ref, *tol["lse"])
+    compare(f"{w.key}:o", o, o_ref, *tol["o"], gate=gate)
+    compare(f"{w.key}:lse", lse, lse_ref, *tol["lse"])
     if not do_bwd:
         return
     dq, dk, dv = run_bwd(inp, w, o, lse)
     dq_ref, dk_ref, dv_ref, _ = oracle.backward(inp["q"], inp["k"], inp["v"], inp["do"],
                                                 w.scale, w.causal, inp["kv_lens"])
-    compare("dq", dq, dq_ref, *tol["grad"])
-    compare("dk", dk, dk_ref, *tol["grad"])
-    compare("dv", dv, dv_ref, *tol["grad"])
+    compare(f"{w.key}:dq", dq, dq_ref, *tol["grad"], gate=gate)
+    compare(f"{w.key}:dk", dk, dk_ref, *tol["grad"], gate=gate)
+    compare(f"{w.key}:dv", dv, dv_ref, *tol["grad"], gate=gate)
 
 
 @pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
@@ -78,7 +80,7 @@ def sample_rows(Sq, n, seed):
 def test_dit_workloads_sampled_rows(key):
     w = workloads.get(key)
     inp = workloads.make_inputs(w)
-    tol = TOL[w.dtype]
+    tol, gate = TOL[w.dtype], GATE[w.dtype]
     o, lse = run_fwd(inp, w, guard=False)
     o = o.cpu()
     lse = lse.cpu()
@@ -91,5 +93,26 @@ def test_dit_workloads_sampled_rows(key):
         o_ref, lse_ref = oracle.forward_rows(inp["q"][:, :, h:h + 1], inp["k"][:, :, kvh:kvh + 1],
                                              inp["v"][:, :, kvh:kvh + 1], w.scale, w.causal,
                                              lens, 0, 0, rows)
-        compare(f"o[h={h}]", o[0, rows, h], o_ref, *tol["o"])
-        compare(f"lse[h={h}]", lse[0, h, rows], lse_ref, *tol["lse"])
+        compare(f"{key}:o[h={h}]", o[0, rows, h], o_ref, *tol["o"], gate=gate)
+        compare(f"{key}:lse[h={h}]", lse[0, h, rows], lse_ref, *tol["lse"])
+
+
+def test_long_kv_work_order_whole_oracle_on_two_heads():
+    """K/V too large for L2 (2 x 49 MB > the 43 MB head-inner limit), so the forward takes
+    its long-K/V work order (consecutive query tiles of one head together) that otherwise
+    only the DiT self-attention sizes reach. Plain N(0,1) Q and K, so |O| ~ 0.1 and the
+    element-wise bound is not vacuous; GQA (two query heads per kv head) and a ragged last
+    query tile (1000 = 7 x 128 + 104). The whole oracle on two heads of different kv heads."""
+    w = workloads.small_case("long_kv", "long_kv_gqa_d128", 1, 8, 4, 1000, 24000, 128, "bf16",
+                             False, seed=4242, has_bwd=False)
+    inp = workloads.make_inputs(w)
+    assert 2 * w.B * w.Hkv * w.Skv * w.D * 2 > 43.0e6
+    tol, gate = TOL[w.dtype], GATE[w.dtype]
+    o, lse = run_fwd(inp, w)
+    o, lse = o.cpu(), lse.cpu()
+    for h in (1, 6):
+        kvh = h // 2
+        o_ref, lse_ref = oracle.forward(inp["q"][:, :, h:h + 1], inp["k"][:, :, kvh:kvh + 1],
+                                        inp["v"][:, :, kvh:kvh + 1], w.scale, w.causal, None)
+        compare(f"long_kv:o[h={h}]", o[:, :, h:h + 1], o_ref, *tol["o"], gate=gate)
+        compare(f"long_kv:lse[h={h}]", lse[:, h:h + 1], lse_ref, *tol["lse"])
