@@ -28,10 +28,12 @@ ATTN_ERR_WORKSPACE = -5
 ATTN_DEVERR_KVLEN = 0x1
 ATTN_DEVERR_TIMEOUT = 0x2
 ATTN_DEVERR_LAYOUT = 0x4
+ATTN_DEVERR_PAGE = 0x8
 
 EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_peek_device_error",
             "attn_status_string", "attn_build_info", "attn_launch_count", "attn_bwd_noalloc",
-            "attn_test_inject_fault", "attn_last_cuda_error")
+            "attn_test_inject_fault", "attn_last_cuda_error", "attn_fwd_paged",
+            "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_size")
 ATTN_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _lib = None
@@ -78,6 +80,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i,
                                      vp, i, vp]
     lib.attn_launch_count.argtypes = []
+    lib.attn_fwd_paged.restype = i
+    lib.attn_fwd_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, i,
+                                   vp]
+    lib.attn_fwd_splitkv.restype = i
+    lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp, sz,
+                                     vp]
+    lib.attn_fwd_splitkv_workspace_size.restype = sz
+    lib.attn_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i, i, i]
     _lib = lib
     return lib
 
@@ -179,6 +189,64 @@ def attn_fwd(q, k, v, o, lse, causal: bool = False, scale: float | None = None,
                          _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd")
+
+
+def attn_fwd_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, causal: bool = False,
+                   scale: float | None = None, stream=None) -> None:
+    """O and LSE of attention over a paged K/V cache. q, o [B,Sq,Hq,D]; k_pages, v_pages
+    [num_pages, page_size, Hkv, D]; block_table int32 [B, max_pages]; seq_lens int32 [B]
+    (or None: every sequence holds max_pages * page_size keys); lse fp32 [B,Hq,Sq]."""
+    _check_cuda(q, k_pages, v_pages, block_table, seq_lens, o, lse)
+    if q.dim() != 4 or k_pages.dim() != 4 or v_pages.shape != k_pages.shape:
+        raise ValueError("q [B,Sq,Hq,D] and page pools [pages, page_size, Hkv, D] expected")
+    B, Sq, Hq, D = q.shape
+    num_pages, page_size, Hkv, Dk = k_pages.shape
+    if Dk != D or k_pages.dtype != q.dtype or v_pages.dtype != q.dtype:
+        raise ValueError("page pools must match q in D and element type")
+    if o.shape != q.shape or o.dtype != q.dtype:
+        raise ValueError("o must have q's shape and element type")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Sq):
+        raise ValueError(f"lse must be float32 {(B, Hq, Sq)}")
+    if (block_table.dtype != torch.int32 or block_table.dim() != 2 or
+            block_table.shape[0] != B):
+        raise ValueError("block_table must be int32 [B, max_pages]")
+    if seq_lens is not None and (seq_lens.dtype != torch.int32 or tuple(seq_lens.shape) != (B,)):
+        raise ValueError("seq_lens must be int32 [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    st = load().attn_fwd_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                               _ptr(seq_lens), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, num_pages,
+                               page_size, block_table.shape[1], D, float(scale),
+                               int(bool(causal)), _dtype_code(q), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_paged")
+
+
+def attn_fwd_splitkv_workspace_size(B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,
+                                    dtype_code: int) -> int:
+    return int(load().attn_fwd_splitkv_workspace_size(B, Hq, Hkv, Sq, Skv, D, dtype_code))
+
+
+def attn_fwd_splitkv(q, k, v, o, lse, causal: bool = False, scale: float | None = None,
+                     kv_lens=None, workspace=None, stream=None) -> None:
+    """attn_fwd for short query blocks over long K/V, with the key range split across work
+    items and the partials merged. ``workspace``: a uint8 device tensor of at least
+    attn_fwd_splitkv_workspace_size() bytes; allocated here (by torch) when None."""
+    _check_cuda(q, k, v, o, lse, kv_lens)
+    _check_shapes(q, k, v, lse, kv_lens, like_q=(("o", o),))
+    B, Sq, Hq, D = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    code = _dtype_code(q)
+    need = attn_fwd_splitkv_workspace_size(B, Hq, Hkv, Sq, Skv, D, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = load().attn_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq,
+                                 Skv, D, float(scale), int(bool(causal)), _ptr(kv_lens), code,
+                                 _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_splitkv")
 
 
 def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,

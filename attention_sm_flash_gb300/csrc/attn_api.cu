@@ -97,6 +97,85 @@ extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, v
   return from_cuda(dtype == ATTN_BF16 ? tc_fwd(p, s) : simt_fwd(p, s));
 }
 
+extern "C" attn_status_t attn_fwd_paged(const void* q, const void* k_pages,
+                                        const void* v_pages, const int32_t* block_table,
+                                        const int32_t* seq_lens, void* o, float* lse, int B,
+                                        int Hq, int Hkv, int Sq, int num_pages, int page_size,
+                                        int max_pages, int D, float scale, int causal,
+                                        attn_dtype_t dtype, attn_stream_t stream) {
+  if (num_pages < 1 || max_pages < 1 || page_size < 1) return ATTN_ERR_INVALID_ARG;
+  const long long skv = (long long)max_pages * page_size;
+  if (skv > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  if (seq_lens != nullptr && !aligned(seq_lens, 4)) return ATTN_ERR_INVALID_ARG;
+  attn_status_t st = check_common(B, Hq, Hkv, Sq, (int)skv, D, scale, causal, nullptr, dtype);
+  if (st != ATTN_OK) return st;
+  if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  // a power of two of at least 16 keys: a 128-key tile is then whole pages or lies inside
+  // one page, and the kernel locates keys with shifts
+  if (page_size < 16 || (page_size & (page_size - 1)) != 0) return ATTN_ERR_UNSUPPORTED;
+  if ((double)num_pages * page_size * Hkv * D > 4.0e18) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || Sq == 0) return ATTN_OK;
+  if (q == nullptr || o == nullptr || lse == nullptr || k_pages == nullptr ||
+      v_pages == nullptr || block_table == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || !aligned(block_table, 4))
+    return ATTN_ERR_INVALID_ARG;
+  Problem p{};
+  p.q = q; p.k = k_pages; p.v = v_pages; p.o = o; p.lse = lse;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = (int)skv; p.D = D;
+  p.scale = scale; p.causal = causal; p.kv_lens = seq_lens; p.dtype = dtype;
+  p.block_table = block_table; p.num_pages = num_pages; p.page_size = page_size;
+  p.max_pages = max_pages;
+  cudaError_t e = error_word(&p.err);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(tc_fwd(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv,
+                                                  int D, attn_dtype_t dtype) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || D <= 0) return 0;
+  int per = 0;
+  const int n = fwd_split_count(B, Hq, Sq, Skv, dtype, &per);
+  if (n <= 1) return 0;
+  return fwd_split_part_bytes(n, B, Hq, Sq, D) + fwd_split_lse_bytes(n, B, Hq, Sq);
+}
+
+extern "C" attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o,
+                                          float* lse, int B, int Hq, int Hkv, int Sq, int Skv,
+                                          int D, float scale, int causal,
+                                          const int32_t* kv_lens, attn_dtype_t dtype,
+                                          void* workspace, size_t workspace_bytes,
+                                          attn_stream_t stream) {
+  attn_status_t st = check_common(B, Hq, Hkv, Sq, Skv, D, scale, causal, kv_lens, dtype);
+  if (st != ATTN_OK) return st;
+  int per = 0;
+  const int n = (B > 0 && Sq > 0) ? fwd_split_count(B, Hq, Sq, Skv, dtype, &per) : 1;
+  if (n <= 1)
+    return attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, scale, causal, kv_lens, dtype,
+                    stream);
+  if (q == nullptr || o == nullptr || lse == nullptr || k == nullptr || v == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_fwd_splitkv_workspace_size(B, Hq, Hkv, Sq, Skv, D, dtype);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+    return ATTN_ERR_WORKSPACE;
+  Problem p{};
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.D = D;
+  p.scale = scale; p.causal = causal; p.kv_lens = kv_lens; p.dtype = dtype;
+  p.fwd_splits = n;
+  p.fwd_split_tiles = per;
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                        fwd_split_part_bytes(n, B, Hq, Sq, D));
+  cudaError_t e = error_word(&p.err);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(tc_fwd(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 extern "C" size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int D,
                                           attn_dtype_t dtype) {
   if (B <= 0 || Hq <= 0 || Sq <= 0 || Hkv <= 0 || Skv < 0 || D <= 0) return 0;
@@ -166,7 +245,7 @@ extern "C" attn_status_t attn_peek_device_error(uint32_t* bits, attn_stream_t st
   if (bits != nullptr) *bits = word;
   if (word & ATTN_DEVERR_TIMEOUT) return ATTN_ERR_TIMEOUT;
   if (word & ATTN_DEVERR_LAYOUT) return ATTN_ERR_CUDA;
-  if (word & ATTN_DEVERR_KVLEN) return ATTN_ERR_INVALID_ARG;
+  if (word & (ATTN_DEVERR_KVLEN | ATTN_DEVERR_PAGE)) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 
@@ -193,5 +272,6 @@ extern "C" const char* attn_last_cuda_error(void) {
 extern "C" uint64_t attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 extern "C" const char* attn_build_info(void) {
-  return "libattn sm_103a: bf16 fwd+bwd tcgen05/TMA/TMEM; fp32 fwd/bwd CUDA-core";
+  return "libattn sm_103a: bf16 fwd (dense, paged, split-KV) + bwd tcgen05/TMA/TMEM; fp32 "
+         "fwd/bwd CUDA-core";
 }

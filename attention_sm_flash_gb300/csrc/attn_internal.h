@@ -28,10 +28,49 @@ struct Problem {
   int B, Hq, Hkv, Sq, Skv, D;
   float scale;
   int causal;
-  const int32_t* kv_lens;  // [B, Hkv] or null
+  const int32_t* kv_lens;  // [B, Hkv] or null; [B] for a paged forward
   attn_dtype_t dtype;
   unsigned int* err;       // device error word (ATTN_DEVERR_* bits)
+  // paged forward (block_table non-null): k, v are page pools [num_pages, page_size, Hkv,
+  // D]; block_table [B, max_pages]; Skv = max_pages * page_size
+  const int32_t* block_table;
+  int num_pages, page_size, max_pages;
+  // split-KV forward (fwd_splits > 1): ranges of fwd_split_tiles key tiles, partial
+  // outputs in the caller's workspace
+  int fwd_splits, fwd_split_tiles;
+  float* o_part;   // [fwd_splits, B, Hq, Sq, D]
+  float* lse_part; // [fwd_splits, B, Hq, Sq]
 };
+
+inline size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+
+// Split-KV forward: into how many key ranges each (batch, head, 128-row query block) is
+// cut, and how many 128-key tiles a range holds. Short query blocks over long K/V (decode,
+// a few query rows against a whole cache) give too few work items to fill the GPU; the
+// ranges multiply them up to about 304 (two per SM of a 152-SM GB300), each range at least
+// 4 tiles long so that an item's fill and drain stay small against its work. 1: no split.
+// A pure function of the sizes, so that the workspace query and the launch agree.
+inline int fwd_split_count(int B, int Hq, int Sq, int Skv, attn_dtype_t dtype, int* tiles_per) {
+  const int tiles = (Skv + 127) / 128;
+  if (tiles_per != nullptr) *tiles_per = tiles;
+  if (dtype != ATTN_BF16 || B <= 0 || Hq <= 0 || Sq <= 0 || Skv <= 0) return 1;
+  const long long base = (long long)B * Hq * ((Sq + 127) / 128);
+  const long long target = 304;
+  if (base >= target / 2) return 1;
+  long long n = (target + base - 1) / base;
+  const long long most = tiles / 4;
+  if (n > most) n = most;
+  if (n <= 1) return 1;
+  const int per = (int)((tiles + n - 1) / n);
+  if (tiles_per != nullptr) *tiles_per = per;
+  return (tiles + per - 1) / per;
+}
+inline size_t fwd_split_part_bytes(int splits, int B, int Hq, int Sq, int D) {
+  return round256((size_t)splits * B * Hq * Sq * D * sizeof(float));
+}
+inline size_t fwd_split_lse_bytes(int splits, int B, int Hq, int Sq) {
+  return round256((size_t)splits * B * Hq * Sq * sizeof(float));
+}
 
 // Into how many parts the bf16 backward splits each GQA group's dK/dV work (0: not
 // split). A (batch, kv head, 128-key tile) work item covers the whole group; when such
@@ -50,7 +89,6 @@ inline int bwd_split_parts(int B, int Hq, int Hkv, int Skv, attn_dtype_t dtype) 
     if (g % d == 0 && items * d >= 256) return d;
   return g;
 }
-inline size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 inline size_t bwd_delta_bytes(int B, int Hq, int Sq) { return round256((size_t)B * Hq * Sq * sizeof(float)); }
 // one fp32 partial dK (or dV) buffer [B, Skv, Hkv * parts, D]
 inline size_t bwd_partial_bytes(int B, int Hkv, int parts, int Skv, int D) {
@@ -67,7 +105,8 @@ cudaError_t simt_bwd(const Problem& p, cudaStream_t stream);
 // (the bf16 backward has a delta kernel of its own).
 cudaError_t simt_delta(const Problem& p, cudaStream_t stream);
 
-// Tensor-core (tcgen05) kernels for bf16, sm_103a.
+// Tensor-core (tcgen05) kernels for bf16, sm_103a. tc_fwd covers the dense, the paged
+// and the split-KV forward (the latter adds the merge kernel).
 cudaError_t tc_fwd(const Problem& p, cudaStream_t stream);
 cudaError_t tc_bwd(const Problem& p, cudaStream_t stream);
 

@@ -49,6 +49,7 @@
 #include <mutex>
 
 #include "attn_internal.h"
+#include "fastdiv.h"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -83,6 +84,11 @@ struct BwdParams {
   int B, Hq, Hkv, Sq, Skv, causal;
   int split;  // parts per GQA group (0: not split)
   int n_items;
+  // the divisions of the work decode, as multiplies (fastdiv.h): dQ items by B * Hq, Hq,
+  // the query tiles n_qt and the group g = Hq / Hkv; dK/dV items by B * Hkv * gs, n_kt * gs,
+  // gs (items per (batch, kv head, key tile)) and Hkv
+  FastDiv fd_bh, fd_hq, fd_nqt, fd_g, fd_bkgs, fd_ktgs, fd_gs, fd_hkv;
+  int heads_per_item;  // g / gs
   float scale, scale_log2;
   uint64_t timeout_ns;
 };
@@ -158,24 +164,24 @@ struct DqItem {
 };
 
 __device__ __forceinline__ DqItem dq_decode(int idx, const BwdParams& p) {
-  const int n_qt = (p.Sq + kT - 1) / kT;
-  const int BH = p.B * p.Hq;
+  const int n_qt = p.fd_nqt.d;
   int b, h, qt;
   if (p.causal) {
-    qt = n_qt - 1 - idx / BH;  // longest first
-    const int bh = idx % BH;
-    b = bh / p.Hq;
-    h = bh % p.Hq;
+    const int r = p.fd_bh.div(idx);
+    qt = n_qt - 1 - r;  // longest first
+    const int bh = idx - r * p.fd_bh.d;
+    b = p.fd_hq.div(bh);
+    h = bh - b * p.Hq;
   } else {
-    const int bh = idx / n_qt;
-    qt = idx % n_qt;
-    b = bh / p.Hq;
-    h = bh % p.Hq;
+    const int bh = p.fd_nqt.div(idx);
+    qt = idx - bh * n_qt;
+    b = p.fd_hq.div(bh);
+    h = bh - b * p.Hq;
   }
   DqItem it;
   it.b = b;
   it.h = h;
-  it.kvh = h / (p.Hq / p.Hkv);
+  it.kvh = p.fd_g.div(h);
   it.q0 = qt * kT;
   it.L = kv_len_of(p, b, it.kvh);
   int kmax = it.L;
@@ -575,33 +581,31 @@ struct DkvItem {
 };
 
 __device__ __forceinline__ DkvItem dkv_decode(int idx, const BwdParams& p) {
-  const int n_kt = (p.Skv + kT - 1) / kT;
-  const int g = p.Hq / p.Hkv;
-  const int gs = p.split ? p.split : 1;  // items per (batch, kv head, key tile)
-  const int BK = p.B * p.Hkv;
+  const int g = p.fd_g.d;
+  const int gs = p.fd_gs.d;  // items per (batch, kv head, key tile)
   int b, kvh, kt, r;
   if (p.causal) {
     // longest first: the first key tiles are seen by the most queries
-    kt = idx / (BK * gs);
-    const int rem = idx % (BK * gs);
-    const int bk = rem / gs;
-    r = rem % gs;
-    b = bk / p.Hkv;
-    kvh = bk % p.Hkv;
+    kt = p.fd_bkgs.div(idx);
+    const int rem = idx - kt * p.fd_bkgs.d;
+    const int bk = p.fd_gs.div(rem);
+    r = rem - bk * gs;
+    b = p.fd_hkv.div(bk);
+    kvh = bk - b * p.Hkv;
   } else {
-    const int bk = idx / (n_kt * gs);
-    const int rem = idx % (n_kt * gs);
-    kt = rem / gs;
-    r = rem % gs;
-    b = bk / p.Hkv;
-    kvh = bk % p.Hkv;
+    const int bk = p.fd_ktgs.div(idx);
+    const int rem = idx - bk * p.fd_ktgs.d;
+    kt = p.fd_gs.div(rem);
+    r = rem - kt * gs;
+    b = p.fd_hkv.div(bk);
+    kvh = bk - b * p.Hkv;
   }
   DkvItem it;
   it.b = b;
   it.kvh = kvh;
   it.j0 = kt * kT;
   it.L = kv_len_of(p, b, kvh);
-  it.heads = g / gs;
+  it.heads = p.heads_per_item;
   it.h0 = kvh * g + r * it.heads;
   it.slot = kvh * gs + r;
   const int n_qt = (p.Sq + kT - 1) / kT;
@@ -705,9 +709,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         load_tile<D>(sV, &p.tm_v, &c.v_full, it.kvh, it.j0, it.b, kT);
       }
       ++v_cnt;
+      // tile t is query tile it.i_start + qi of query head it.h0 + hh, kept as running
+      // counters: a division by the per-item per_head would go through the MUFU
+      // reciprocal, which the exponentials of the elementwise warps keep busy
+      int hh = 0, qi = -1;
       for (int t = 0; t < it.n_tiles; ++t) {
-        const int h = it.h0 + t / it.per_head;
-        const int i0 = (it.i_start + t % it.per_head) * kT;
+        if (++qi == it.per_head) {
+          qi = 0;
+          ++hh;
+        }
+        const int h = it.h0 + hh;
+        const int i0 = (it.i_start + qi) * kT;
         // dO first: its stage slot is released earlier in the tile than Q's
         if (!wait_phase_warp(&c.do_empty[st], st_par ^ 1, wc)) { ok = false; break; }
         if (lane == 0) {
@@ -868,7 +880,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         }
         continue;
       }
+      int qi = -1;  // query tile of tile t within its head (a running counter, no division)
       for (int t = 0; t < it.n_tiles; ++t, ++gt) {
+        if (++qi == it.per_head) qi = 0;
         const uint32_t s = gt % NST;
         if (!wait_phase_warp(&c.q_full[s], (gt / NST) & 1, wc)) { ok = false; break; }
         // the tile's per-column -LSE go to registers before the wait for S^T: while SS MMAs
@@ -879,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         for (int e = 0; e < 16; ++e) nlv[e] = reinterpret_cast<const float4*>(&c.nlse[s][64 * hsel])[e];
         if (!wait_phase_warp(&c.s_full, gt & 1, wc)) { ok = false; break; }
         tc_fence_after();
-        const int i0 = (it.i_start + t % it.per_head) * kT + 64 * hsel;
+        const int i0 = (it.i_start + qi) * kT + 64 * hsel;
         // causal: key j is visible to query i0 + e iff e >= j - L + Sq - i0
         const int qlo = p.causal ? j - it.L + p.Sq - i0 : -1;
         const float2* nlq = reinterpret_cast<const float2*>(nlv);
@@ -1143,6 +1157,19 @@ cudaError_t launch_bwd(const Problem& p, int dev, cudaStream_t s) {
   prm.scale = p.scale;
   prm.scale_log2 = p.scale * kLog2e;
   prm.timeout_ns = 4000000000ull;
+  {
+    const int g = p.Hq / p.Hkv, gs = p.split ? p.split : 1;
+    const int n_qt = (p.Sq + kT - 1) / kT, n_kt = (p.Skv + kT - 1) / kT;
+    prm.fd_bh = FastDiv::make(p.B * p.Hq);
+    prm.fd_hq = FastDiv::make(p.Hq);
+    prm.fd_nqt = FastDiv::make(n_qt);
+    prm.fd_g = FastDiv::make(g);
+    prm.fd_bkgs = FastDiv::make(p.B * p.Hkv * gs);
+    prm.fd_ktgs = FastDiv::make(n_kt * gs);
+    prm.fd_gs = FastDiv::make(gs);
+    prm.fd_hkv = FastDiv::make(p.Hkv);
+    prm.heads_per_item = g / gs;
+  }
   const int sms = g_num_sms[dev];
   {
     const int64_t threads = (int64_t)p.B * p.Sq * p.Hq * (D / 8);

@@ -37,6 +37,7 @@
 #include <mutex>
 
 #include "attn_internal.h"
+#include "fastdiv.h"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -51,17 +52,39 @@ constexpr int kThreads = 384;    // warps 0-3: producer, S issuer, V fixer, PV i
 constexpr int kSoftThreads = 256;
 constexpr int kMaxSortedHeads = 64;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows > 2^8
+// Kernel kinds, a template parameter so that each is compiled without the others' code:
+// dense K/V, a paged K/V cache, and split-KV items writing partials.
+constexpr int kDense = 0, kPaged = 1, kSplit = 2;
 
 struct FwdParams {
   CUtensorMap tm_q;
   CUtensorMap tm_o;  // O, same layout and box as Q (the epilogue's tile stores)
-  CUtensorMap tm_k;
+  CUtensorMap tm_k;  // dense [B, Skv, Hkv, D], or the page pool [pages, page_size, Hkv, D]
   CUtensorMap tm_v;
   __nv_bfloat16* o;
   float* lse;
   const int32_t* kv_lens;
+  int lens_bstride, lens_hstride;  // valid length of (b, kvh) = kv_lens[b * bs + kvh * hs]
   unsigned int* err;
+  // paged K/V (block_table non-null): key t of sequence b is row t % page_size of page
+  // block_table[b * max_pages + t / page_size]; Skv = max_pages * page_size
+  const int32_t* block_table;
+  int max_pages, num_pages;
+  // page_size = 1 << page_shift; page_box = 1 << box_shift rows per TMA box. Powers of two,
+  // so the producer works with shifts: an integer division by a runtime value needs the
+  // MUFU reciprocal, whose queue the softmax's exponentials keep full (measured: several
+  // hundred cycles per box on the producer's critical path)
+  int page_shift, box_shift;
+  // split-KV: each (b, h, q block) is n_splits items over consecutive ranges of
+  // split_tiles key tiles; an item writes its normalised partial O and LSE (fp32) and
+  // fwd_combine_kernel merges them
+  int n_splits, split_tiles;
+  float* o_part;    // [n_splits, B, Hq, Sq, D]
+  float* lse_part;  // [n_splits, B, Hq, Sq]
   int B, Hq, Hkv, Sq, Skv;
+  // the divisions of the work decode, as multiplies (fastdiv.h): by n_splits, B * Hq,
+  // Hq, Hkv, n_qblocks, the GQA group g = Hq / Hkv and g * n_qblocks
+  FastDiv fd_splits, fd_bh, fd_hq, fd_hkv, fd_qb, fd_g, fd_per;
   int causal;
   int head_inner;    // non-causal order with the (batch, head) index innermost
   int n_qblocks;
@@ -92,58 +115,73 @@ struct FwdCtl {
 
 struct Item {
   int b, h, kvh, q0, L;
-  int n;  // K/V tiles the Q tile visits
+  int j0;     // first K/V tile
+  int n;      // K/V tiles the item visits: j0 .. j0 + n - 1
+  int split;  // key range of a split-KV item (0 otherwise)
 };
 
 __device__ __forceinline__ int clamp_len(int L, int Skv) { return L < 0 ? 0 : (L > Skv ? Skv : L); }
 
-template <typename Ctl>
+__device__ __forceinline__ int len_at(const FwdParams& p, int b, int kvh) {
+  return __ldg(p.kv_lens + b * p.lens_bstride + kvh * p.lens_hstride);
+}
+
+template <int KIND, typename Ctl>
 __device__ __forceinline__ Item decode_item(int idx, const FwdParams& p, const Ctl& c) {
-  const int g = p.Hq / p.Hkv;
+  const int g = p.fd_g.d;
+  int split = 0;
+  if (KIND == kSplit) {
+    const int rest = p.fd_splits.div(idx);
+    split = idx - rest * p.n_splits;
+    idx = rest;
+  }
   int b, h, qb;
   if (p.causal) {
     // longest first: the last query blocks see the most keys
-    const int BH = p.B * p.Hq;
-    qb = p.n_qblocks - 1 - idx / BH;
-    const int bh = idx % BH;
-    b = bh / p.Hq;
-    h = bh % p.Hq;
+    const int r = p.fd_bh.div(idx);
+    qb = p.n_qblocks - 1 - r;
+    const int bh = idx - r * p.fd_bh.d;
+    b = p.fd_hq.div(bh);
+    h = bh - b * p.Hq;
   } else if (c.n_sorted > 0) {
     // varlen: (batch, kv head) groups in decreasing valid length
-    const int per = g * p.n_qblocks;
-    const int bk = c.sorted[idx / per];
-    const int rem = idx % per;
-    b = bk / p.Hkv;
-    h = (bk % p.Hkv) * g + rem / p.n_qblocks;
-    qb = rem % p.n_qblocks;
+    const int gi = p.fd_per.div(idx);
+    const int bk = c.sorted[gi];
+    const int rem = idx - gi * p.fd_per.d;
+    b = p.fd_hkv.div(bk);
+    const int hb = p.fd_qb.div(rem);
+    h = (bk - b * p.Hkv) * g + hb;
+    qb = rem - hb * p.n_qblocks;
   } else if (p.head_inner) {
     // short K/V (L2-resident): concurrent CTAs cover every head of the same query rows,
     // so Q is read and O written as whole contiguous rows across heads
-    const int BH = p.B * p.Hq;
-    qb = idx / BH;
-    const int bh = idx % BH;
-    b = bh / p.Hq;
-    h = bh % p.Hq;
+    qb = p.fd_bh.div(idx);
+    const int bh = idx - qb * p.fd_bh.d;
+    b = p.fd_hq.div(bh);
+    h = bh - b * p.Hq;
   } else {
     // long K/V: consecutive query blocks of one head run together and share K/V in L2
-    const int bh = idx / p.n_qblocks;
-    qb = idx % p.n_qblocks;
-    b = bh / p.Hq;
-    h = bh % p.Hq;
+    const int bh = p.fd_qb.div(idx);
+    qb = idx - bh * p.n_qblocks;
+    b = p.fd_hq.div(bh);
+    h = bh - b * p.Hq;
   }
   Item it;
   it.b = b;
   it.h = h;
-  it.kvh = h / g;
+  it.kvh = p.fd_g.div(h);
   it.q0 = qb * kItemRows;
-  it.L = p.kv_lens ? clamp_len(__ldg(p.kv_lens + b * p.Hkv + it.kvh), p.Skv) : p.Skv;
+  it.L = p.kv_lens ? clamp_len(len_at(p, b, it.kvh), p.Skv) : p.Skv;
   int kmax = it.L;
   if (p.causal) {
     const int ilast = min(it.q0 + kBM - 1, p.Sq - 1);
     kmax = min(it.L, ilast + it.L - p.Sq + 1);
   }
   kmax = max(kmax, 0);
-  it.n = (kmax + kBN - 1) / kBN;
+  const int tiles = (kmax + kBN - 1) / kBN;
+  it.split = split;
+  it.j0 = KIND == kSplit ? split * p.split_tiles : 0;
+  it.n = KIND == kSplit ? max(0, min(p.split_tiles, tiles - it.j0)) : tiles;
   return it;
 }
 
@@ -160,7 +198,7 @@ __device__ __forceinline__ int pv_steps(int j, int L) {
   return (valid + 15) / 16;
 }
 
-template <int D, int NQ, int NK, int NV>
+template <int D, int NQ, int NK, int NV, int KIND>
 __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
   constexpr int kQTile = kBM * D * 2;     // bytes of a Q tile
   constexpr int kKVTile = kBN * D * 2;    // bytes of a K or V tile
@@ -184,6 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
   Ctl& c = *reinterpret_cast<Ctl*>(sO + kQTile);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // split-KV: the merge that follows is a programmatic dependent of this grid (it waits
+  // for this grid's completion before reading the partials), so its launch overlaps
+  if (KIND == kSplit) griddep_launch_dependents();
 
   // ------------------------------------------------------------------- prologue
   if (threadIdx.x == 0) {
@@ -228,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
   const bool sort_heads = !p.causal && p.kv_lens != nullptr && nbk <= kMaxSortedHeads;
   if (p.kv_lens != nullptr) {
     for (int e = threadIdx.x; e < nbk; e += kThreads) {
-      const int raw = __ldg(p.kv_lens + e);
+      const int raw = len_at(p, e / p.Hkv, e % p.Hkv);
       if ((raw < 0 || raw > p.Skv) && blockIdx.x == 0) atomicOr(p.err, ATTN_DEVERR_KVLEN);
       if (sort_heads) c.lens[e] = clamp_len(raw, p.Skv);
     }
@@ -259,6 +300,53 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
       tma_prefetch_map(&p.tm_k);
       tma_prefetch_map(&p.tm_v);
     }
+    // Paged K/V: block-table entries are read 32 at a time, one per lane, and handed out
+    // by shuffles, so the producer does not wait for a global load before every tile. One
+    // cache for K and one for V (K runs ahead of V); reset at every item.
+    struct PageCache {
+      int base, val;
+    };
+    PageCache pc_k{-1, 0}, pc_v{-1, 0};
+    auto page_of = [&](PageCache& pc, int b, int e) -> int {  // warp-uniform e
+      if (pc.base < 0 || e < pc.base || e >= pc.base + 32) {
+        pc.base = e;
+        pc.val = e + lane < p.max_pages ? __ldg(p.block_table + (int64_t)b * p.max_pages + e + lane) : 0;
+      }
+      return __shfl_sync(0xffffffffu, pc.val, e - pc.base);
+    };
+    // K/V tile jj of an item into `dst`, completing on `bar`; called by the whole warp,
+    // lane 0 issues. Dense: one box of 128 keys per 64-column chunk. Paged: the tile's keys
+    // in boxes of page_box rows, each inside one page; boxes that start at or past the
+    // valid length are not loaded (their keys are masked, and the V rows that the PV
+    // product reads there are zeroed by warp 2).
+    auto load_kv = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int jj, const Item& it,
+                       PageCache& pc) {
+      if constexpr (KIND != kPaged) {
+        if (lane == 0) {
+          mbar_expect_tx(bar, kKVTile);
+          for (int ch = 0; ch < kChunks; ++ch)
+            tma_load_4d(dst + ch * kKVChunk, map, bar, ch * 64, it.kvh, jj * kBN, it.b);
+        }
+      } else {
+        const int valid = min(kBN, it.L - jj * kBN);  // >= 1: tile jj holds valid keys
+        const int box = 1 << p.box_shift;
+        const int boxes = (valid + box - 1) >> p.box_shift;
+        if (lane == 0) mbar_expect_tx(bar, (uint32_t)(boxes << p.box_shift) * 128 * kChunks);
+        for (int x = 0; x < boxes; ++x) {
+          const int t0 = jj * kBN + (x << p.box_shift);
+          int page = page_of(pc, it.b, t0 >> p.page_shift);
+          if (lane == 0) {
+            if (page < 0 || page >= p.num_pages) {
+              atomicOr(p.err, ATTN_DEVERR_PAGE);
+              page = 0;  // a page that exists: the call's outputs are invalid, nothing faults
+            }
+            for (int ch = 0; ch < kChunks; ++ch)
+              tma_load_4d(dst + ch * kKVChunk + (x << p.box_shift) * 128, map, bar, ch * 64, it.kvh,
+                          t0 & ((1 << p.page_shift) - 1), page);
+          }
+        }
+      }
+    };
     // K_j is read by S(j), which runs up to two tiles ahead of PV(j); so K is loaded two
     // tiles ahead of V and kept on its own ring, freed as soon as S(j) completes
     uint32_t kpos = 0, vpos = 0, qs = 0, q_par = 0;
@@ -266,8 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
     uint32_t q_issued = 0, q_last = 0;                      // per Q slot
     bool ok = true, first = true;
     for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-      const Item it = decode_item(idx, p, c);
+      const Item it = decode_item<KIND>(idx, p, c);
       if (it.n == 0) continue;
+      pc_k.base = -1;  // a new sequence: its block-table row
+      pc_v.base = -1;
       if (!wait_phase_warp(&c.q_empty[qs], q_par ^ 1, wc)) { ok = false; break; }
       if (lane == 0) {
         mbar_expect_tx(&c.q_full[qs], kQTile);
@@ -284,12 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
           if (!wait_phase_warp(&c.k_empty[ks], kpar ^ 1, wc)) { ok = false; break; }
           const bool skip = (p.fault & 1u) && blockIdx.x == 0 && first && j == 0;
           if (!skip) {
-            if (lane == 0) {
-              mbar_expect_tx(&c.k_full[ks], kKVTile);
-              for (int ch = 0; ch < kChunks; ++ch)
-                tma_load_4d(sK + ks * kKVTile + ch * kKVChunk, &p.tm_k, &c.k_full[ks], ch * 64, it.kvh,
-                            j * kBN, it.b);
-            }
+            load_kv(sK + ks * kKVTile, &p.tm_k, &c.k_full[ks], it.j0 + j, it, pc_k);
             k_iss |= 1u << ks;
             k_last = (k_last & ~(1u << ks)) | (kpar << ks);
           }
@@ -299,16 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
           const int j = step - 2;
           const uint32_t vs = vpos % NV, vpar = (vpos / NV) & 1;
           if (!wait_phase_warp(&c.v_empty[vs], vpar ^ 1, wc)) { ok = false; break; }
-          if (lane == 0) {
-            mbar_expect_tx(&c.v_full[vs], kKVTile);
-            for (int ch = 0; ch < kChunks; ++ch)
-              tma_load_4d(sV + vs * kKVTile + ch * kKVChunk, &p.tm_v, &c.v_full[vs], ch * 64, it.kvh,
-                          j * kBN, it.b);
-          }
+          load_kv(sV + vs * kKVTile, &p.tm_v, &c.v_full[vs], it.j0 + j, it, pc_v);
           v_iss |= 1u << vs;
           v_last = (v_last & ~(1u << vs)) | (vpar << vs);
           // a V tile with padding rows: warp 2 zeroes them once the tile has landed
-          if (needs_fix(j, it.L, p.Skv) && lane == 0) mbar_arrive(&c.fix_req[vs]);
+          if (needs_fix(it.j0 + j, it.L, p.Skv) && lane == 0) mbar_arrive(&c.fix_req[vs]);
           ++vpos;
         }
       }
@@ -361,9 +441,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
         ++gs;
         return true;
       };
-      auto issue_pv = [&](int j, int L) -> bool {
+      // PV of the item's tile j (local index), key tile jj = j0 + j of the sequence
+      auto issue_pv = [&](int j, int jj, int L) -> bool {
         const uint32_t vpos = kbase + j, vs = vpos % NV;
-        if (needs_fix(j, L, p.Skv)) {
+        if (needs_fix(jj, L, p.Skv)) {
           if (!wait_phase(&c.v_fixed[vs], (fix_par >> vs) & 1, wc)) return false;
           fix_par ^= 1u << vs;
         } else if (!wait_phase(&c.v_full[vs], (vpos / NV) & 1, wc)) {
@@ -372,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
         if (!wait_phase(&c.p_full[gp & 1], (gp >> 1) & 1, wc)) return false;
         if (j == 0 && !wait_phase(&c.o_free, (ic & 1) ^ 1, wc)) return false;
         tc_fence_after();
-        const int steps = pv_steps(j, L);
+        const int steps = pv_steps(jj, L);
         const uint64_t b0 = desc_v0 + ((vs * kKVTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
@@ -386,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
         return true;
       };
       for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-        const Item it = decode_item(idx, p, c);
+        const Item it = decode_item<KIND>(idx, p, c);
         if (it.n == 0) continue;
         const uint32_t qslot = qpos % NQ;
         if (s_role && !wait_phase(&c.q_full[qslot], (qpos / NQ) & 1, wc)) { ok = false; break; }
@@ -399,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
           mma_commit(&c.q_empty[qslot]);  // last read of Q
         } else {
           // PV(t) once the softmax has written P(t)
-          for (int t = 0; ok && t < it.n; ++t) ok = issue_pv(t, it.L);
+          for (int t = 0; ok && t < it.n; ++t) ok = issue_pv(t, it.j0 + t, it.L);
           if (!ok) break;
         }
         kbase += it.n;
@@ -418,18 +499,19 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
     uint32_t kbase = 0, fr_par = 0;
     bool ok = true;
     for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-      const Item it = decode_item(idx, p, c);
+      const Item it = decode_item<KIND>(idx, p, c);
       if (it.n == 0) continue;
       for (int j = 0; j < it.n; ++j) {
-        if (!needs_fix(j, it.L, p.Skv)) continue;
+        const int jj = it.j0 + j;
+        if (!needs_fix(jj, it.L, p.Skv)) continue;
         const uint32_t vpos = kbase + j, vs = vpos % NV;
         if (!wait_phase_warp(&c.fix_req[vs], (fr_par >> vs) & 1, wc)) { ok = false; break; }
         fr_par ^= 1u << vs;
         if (!wait_phase_warp(&c.v_full[vs], (vpos / NV) & 1, wc)) { ok = false; break; }
-        const int r0 = it.L - j * kBN;  // first padding row (>= 1: tile j holds valid keys)
+        const int r0 = it.L - jj * kBN;  // first padding row (>= 1: tile jj holds valid keys)
         // the PV product reads whole 16-key steps up to the last valid key: only padding
         // rows inside that last step are read, and only they are zeroed
-        const int r1 = pv_steps(j, it.L) * 16;
+        const int r1 = pv_steps(jj, it.L) * 16;
         const int units = (r1 - r0) * kChunks * 8;
         uint8_t* base = sV + vs * kKVTile;
         for (int e = lane; e < units; e += 32) {
@@ -473,16 +555,25 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
       return true;
     };
     for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-      const Item it = decode_item(idx, p, c);
+      const Item it = decode_item<KIND>(idx, p, c);
       const int i = it.q0 + r;
       const bool row_ok = i < p.Sq;
       __nv_bfloat16* orow = p.o + ((static_cast<int64_t>(it.b) * p.Sq + i) * p.Hq + it.h) * D + h * (D / 2);
       float* lrow = p.lse + (static_cast<int64_t>(it.b) * p.Hq + it.h) * p.Sq + i;
+      // split-KV items write their normalised partial O and LSE (fp32) instead
+      const int64_t prow = ((static_cast<int64_t>(it.split) * p.B + it.b) * p.Hq + it.h) * p.Sq + i;
+      float* porow = KIND == kSplit ? p.o_part + prow * D + h * (D / 2) : nullptr;
       if (it.n == 0) {
         if (row_ok) {
-          for (int d = 0; d < D / 2; d += 8)
-            *reinterpret_cast<uint4*>(orow + d) = make_uint4(0u, 0u, 0u, 0u);
-          if (h == 0) *lrow = -CUDART_INF_F;
+          if (KIND == kSplit) {
+            for (int d = 0; d < D / 2; d += 4)
+              *reinterpret_cast<float4*>(porow + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (h == 0) p.lse_part[prow] = -CUDART_INF_F;
+          } else {
+            for (int d = 0; d < D / 2; d += 8)
+              *reinterpret_cast<uint4*>(orow + d) = make_uint4(0u, 0u, 0u, 0u);
+            if (h == 0) *lrow = -CUDART_INF_F;
+          }
         }
         continue;
       }
@@ -494,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
         if (!wait_phase_warp(&c.s_full[b], (g >> 1) & 1, wc)) { ok = false; break; }
         tc_fence_after();
         // visible columns of this half: e < limit
-        const int limit = kend - j * kBN - 64 * h;
+        const int limit = kend - (it.j0 + j) * kBN - 64 * h;
         // one TMEM round trip: this half of the S row into registers, which (with the
         // other half) frees the buffer for S(j + 2)
         float s[64];
@@ -590,6 +681,26 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
       if (!wait_phase_warp(&c.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, wc)) { ok = false; break; }
       tc_fence_after();
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float lse_nat = lt > 0.f ? (m + __log2f(lt)) * 0.69314718055994531f : -CUDART_INF_F;
+      if (KIND == kSplit) {
+        // a split-KV partial: this half row of O / l in fp32 (32-byte stores, the row is
+        // contiguous and 512-byte aligned), then its LSE; fwd_combine_kernel merges them
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+          uint32_t ov[32];
+          tmem_ld32(tO + cc * 32, ov);
+          if (row_ok) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * inv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) st_global_v8(porow + cc * 32 + e * 8, ov + 8 * e);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&c.o_free);
+        if (row_ok && h == 0) p.lse_part[prow] = lse_nat;
+        continue;
+      }
       // O goes out through shared memory and TMA tile stores: written straight from the
       // registers, each thread's row slice would be 16-byte stores 32 rows apart. The
       // staging tile is free once the previous item's store has read it.
@@ -616,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
       mbar_arrive(&c.o_free);  // O's columns may be overwritten
       fence_proxy_async_smem();
       mbar_arrive(&c.o_staged);
-      if (row_ok && h == 0) *lrow = lt > 0.f ? (m + __log2f(lt)) * 0.69314718055994531f : -CUDART_INF_F;
+      if (row_ok && h == 0) *lrow = lse_nat;
       if (warp == 4) {
         if (!wait_phase_warp(&c.o_staged, ic_s & 1, wc)) { ok = false; break; }
         if (lane == 0) {
@@ -643,6 +754,64 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
   }
 }
 
+// The merge of split-KV partials: one warp per query row (b, h, i). With lse_s and O_s
+// the partial LSE and normalised output of key range s (lse_s = -inf for a range with no
+// visible key), lse = m + log(sum_s exp(lse_s - m)), m = max_s lse_s, and
+// O = sum_s exp(lse_s - lse) O_s, summed in range order (deterministic); a row with no
+// visible key at all gets O = 0, lse = -inf. Launched as a programmatic dependent of the
+// forward grid.
+template <int D>
+__global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restrict__ o_part,
+                                                          const float* __restrict__ lse_part,
+                                                          __nv_bfloat16* __restrict__ o,
+                                                          float* __restrict__ lse, int B, int Hq,
+                                                          int Sq, int n_splits) {
+  constexpr int kPer = D / 32;  // columns per lane
+  griddep_wait();
+  const int64_t rows = (int64_t)B * Hq * Sq;
+  const int64_t row = (int64_t)blockIdx.x * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= rows) return;
+  float m = -CUDART_INF_F;
+  for (int sp = lane; sp < n_splits; sp += 32) m = fmaxf(m, lse_part[sp * rows + row]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (m != -CUDART_INF_F) {
+    for (int sp = 0; sp < n_splits; ++sp) {
+      const float ls = lse_part[sp * rows + row];
+      if (ls == -CUDART_INF_F) continue;
+      const float wgt = expf(ls - m);
+      wsum += wgt;
+      const float* src = o_part + (sp * rows + row) * D + lane * kPer;
+      if constexpr (kPer == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        acc[0] += wgt * x.x; acc[1] += wgt * x.y; acc[2] += wgt * x.z; acc[3] += wgt * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] += wgt * x.x; acc[1] += wgt * x.y;
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const int i = (int)(row % Sq);
+  const int64_t bh = row / Sq;
+  const int h = (int)(bh % Hq), b = (int)(bh / Hq);
+  __nv_bfloat16* dst = o + (((int64_t)b * Sq + i) * Hq + h) * D + lane * kPer;
+  uint32_t pk[kPer / 2];
+#pragma unroll
+  for (int e = 0; e < kPer / 2; ++e) pk[e] = pack_bf16x2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+  if constexpr (kPer == 4) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pk[0];
+  }
+  if (lane == 0) lse[row] = wsum > 0.f ? m + logf(wsum) : -CUDART_INF_F;
+}
+
 // ---------------------------------------------------------------------- host side
 template <int D, int NQ, int NK, int NV>
 constexpr size_t fwd_smem_bytes() {
@@ -652,24 +821,42 @@ constexpr size_t fwd_smem_bytes() {
 constexpr int kMaxDev = 64;
 std::mutex g_mu;
 int g_num_sms[kMaxDev] = {};
-bool g_attr_set[kMaxDev][2] = {};
+bool g_attr_set[kMaxDev][2][3] = {};
 
-template <int D, int NQ, int NK, int NV>
+template <int D, int NQ, int NK, int NV, int KIND>
 cudaError_t launch(const FwdParams& prm, int dev, cudaStream_t s) {
   constexpr size_t smem = fwd_smem_bytes<D, NQ, NK, NV>();
   static_assert(smem <= 232448, "shared memory per block");
   {
     std::lock_guard<std::mutex> lk(g_mu);
     const int which = D == 64 ? 0 : 1;
-    if (!g_attr_set[dev][which]) {
-      cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D, NQ, NK, NV>,
+    if (!g_attr_set[dev][which][KIND]) {
+      cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D, NQ, NK, NV, KIND>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
-      g_attr_set[dev][which] = true;
+      g_attr_set[dev][which][KIND] = true;
     }
   }
   const int grid = prm.n_items < g_num_sms[dev] ? prm.n_items : g_num_sms[dev];
-  fwd_sm103_kernel<D, NQ, NK, NV><<<grid, kThreads, smem, s>>>(prm);
+  fwd_sm103_kernel<D, NQ, NK, NV, KIND><<<grid, kThreads, smem, s>>>(prm);
+  count_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || KIND != kSplit) return e;
+  const int64_t rows = (int64_t)prm.B * prm.Hq * prm.Sq;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, fwd_combine_kernel<D>, static_cast<const float*>(prm.o_part),
+                         static_cast<const float*>(prm.lse_part), prm.o, prm.lse, prm.B, prm.Hq,
+                         prm.Sq, prm.n_splits);
+  if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
 }
@@ -719,6 +906,24 @@ void tc_set_test_fault(uint32_t mask, uint64_t timeout_ns) {
   g_fault_timeout_ns = timeout_ns;
 }
 
+// A bf16 page pool [num_pages, page_size, H, D] as a 4-D TMA map (D, H, page_size,
+// num_pages) whose box is one head: 64 columns (128 bytes, 128-byte swizzle) x `rows`
+// keys of one page.
+bool make_page_map(CUtensorMap* map, const void* base, int num_pages, int page_size, int H, int D,
+                   int rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)page_size,
+                              (cuuint64_t)num_pages};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
+                                 (cuuint64_t)page_size * H * D * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -732,18 +937,34 @@ cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
     }
   }
   FwdParams prm{};
+  const bool paged = p.block_table != nullptr;
   // with no keys the K/V maps are never used; describe q so that encoding succeeds
   const bool no_keys = p.Skv == 0;
-  if (!make_bshd_map(&prm.tm_q, p.q, p.B, p.Sq, p.Hq, p.D, kBM) ||
-      !make_bshd_map(&prm.tm_o, p.o, p.B, p.Sq, p.Hq, p.D, kBM) ||
-      !make_bshd_map(&prm.tm_k, no_keys ? p.q : p.k, p.B, no_keys ? p.Sq : p.Skv,
-                no_keys ? p.Hq : p.Hkv, p.D, kBN) ||
-      !make_bshd_map(&prm.tm_v, no_keys ? p.q : p.v, p.B, no_keys ? p.Sq : p.Skv,
-                no_keys ? p.Hq : p.Hkv, p.D, kBN))
-    return cudaErrorInvalidValue;
+  bool maps_ok = make_bshd_map(&prm.tm_q, p.q, p.B, p.Sq, p.Hq, p.D, kBM) &&
+                 make_bshd_map(&prm.tm_o, p.o, p.B, p.Sq, p.Hq, p.D, kBM);
+  if (paged && !no_keys) {
+    const int box = p.page_size < kBN ? p.page_size : kBN;
+    maps_ok = maps_ok && make_page_map(&prm.tm_k, p.k, p.num_pages, p.page_size, p.Hkv, p.D, box) &&
+              make_page_map(&prm.tm_v, p.v, p.num_pages, p.page_size, p.Hkv, p.D, box);
+    while ((1 << prm.page_shift) < p.page_size) ++prm.page_shift;
+    while ((1 << prm.box_shift) < box) ++prm.box_shift;
+  } else {
+    maps_ok = maps_ok &&
+              make_bshd_map(&prm.tm_k, no_keys ? p.q : p.k, p.B, no_keys ? p.Sq : p.Skv,
+                            no_keys ? p.Hq : p.Hkv, p.D, kBN) &&
+              make_bshd_map(&prm.tm_v, no_keys ? p.q : p.v, p.B, no_keys ? p.Sq : p.Skv,
+                            no_keys ? p.Hq : p.Hkv, p.D, kBN);
+  }
+  if (!maps_ok) return cudaErrorInvalidValue;
   prm.o = static_cast<__nv_bfloat16*>(p.o);
   prm.lse = p.lse;
   prm.kv_lens = p.kv_lens;
+  // a paged cache has one valid length per sequence, shared by its kv heads
+  prm.lens_bstride = paged ? 1 : p.Hkv;
+  prm.lens_hstride = paged ? 0 : 1;
+  prm.block_table = paged ? p.block_table : nullptr;
+  prm.max_pages = p.max_pages;
+  prm.num_pages = p.num_pages;
   prm.err = p.err;
   prm.B = p.B;
   prm.Hq = p.Hq;
@@ -754,7 +975,19 @@ cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
   // K/V of every head small enough to stay in L2 (a third of its 129 MB)
   prm.head_inner = (double)p.B * p.Hkv * p.Skv * p.D * 2 * 2 <= 43.0e6 ? 1 : 0;
   prm.n_qblocks = (p.Sq + kItemRows - 1) / kItemRows;
-  prm.n_items = p.B * p.Hq * prm.n_qblocks;
+  prm.n_splits = p.fwd_splits > 1 ? p.fwd_splits : 1;
+  prm.split_tiles = p.fwd_split_tiles;
+  prm.o_part = p.o_part;
+  prm.lse_part = p.lse_part;
+  prm.n_items = p.B * p.Hq * prm.n_qblocks * prm.n_splits;
+  const int g = p.Hq / p.Hkv;
+  prm.fd_splits = FastDiv::make(prm.n_splits);
+  prm.fd_bh = FastDiv::make(p.B * p.Hq);
+  prm.fd_hq = FastDiv::make(p.Hq);
+  prm.fd_hkv = FastDiv::make(p.Hkv);
+  prm.fd_qb = FastDiv::make(prm.n_qblocks);
+  prm.fd_g = FastDiv::make(g);
+  prm.fd_per = FastDiv::make(g * prm.n_qblocks);
   prm.scale_log2 = p.scale * 1.4426950408889634f;
   prm.timeout_ns = 4000000000ull;
   {
@@ -763,8 +996,15 @@ cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
     if (g_fault_next != 0 && g_fault_timeout_ns != 0) prm.timeout_ns = g_fault_timeout_ns;
     g_fault_next = 0;
   }
-  if (p.D == 64) return launch<64, 3, 5, 4>(prm, dev, s);
-  return launch<128, 2, 2, 2>(prm, dev, s);
+  const int kind = paged ? kPaged : (prm.n_splits > 1 ? kSplit : kDense);
+  if (p.D == 64) {
+    if (kind == kPaged) return launch<64, 3, 5, 4, kPaged>(prm, dev, s);
+    if (kind == kSplit) return launch<64, 3, 5, 4, kSplit>(prm, dev, s);
+    return launch<64, 3, 5, 4, kDense>(prm, dev, s);
+  }
+  if (kind == kPaged) return launch<128, 2, 2, 2, kPaged>(prm, dev, s);
+  if (kind == kSplit) return launch<128, 2, 2, 2, kSplit>(prm, dev, s);
+  return launch<128, 2, 2, 2, kDense>(prm, dev, s);
 }
 
 }  // namespace attn

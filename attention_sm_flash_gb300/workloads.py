@@ -34,7 +34,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "get", "make_inputs", "small_case"]
+__all__ = ["Workload", "WORKLOADS", "get", "make_inputs", "small_case", "make_paged"]
 
 
 @dataclass(frozen=True)
@@ -90,6 +90,13 @@ WORKLOADS = {
     # a 28080-token KV cache, 40 heads): context for its FA3 figure, not a graded workload
     "ctx": Workload("ctx", "page_dit_self_q4680_k28080_h40_d128", 1, 40, 40, 4680, 28080, 128,
                     "bf16", False, 20268, qk_factor=0.5),
+    # short query blocks over the DiT self-attention's K/V cache (32760 tokens, 40 heads):
+    # single-query decode (causal, bottom-right: the query sees every key, the last causal
+    # row of xtrain's decode milestone) and 64 query rows; the split-KV forward's cases
+    "dec1": Workload("dec1", "decode_sq1_over_dit_cache_h40_s32760_d128", 1, 40, 40, 1, 32760,
+                     128, "bf16", True, 20269, qk_factor=0.5),
+    "sq64": Workload("sq64", "sq64_over_dit_cache_h40_s32760_d128", 1, 40, 40, 64, 32760, 128,
+                     "bf16", False, 20270, qk_factor=0.5),
     # profiling cases: the same kernels at sizes an ncu capture replays quickly, with
     # inputs still larger than L2 (129 MB)
     "p_self": Workload("p_self", "profile_self_s16384_h16_d128", 1, 16, 16, 16384, 16384, 128,
@@ -144,3 +151,36 @@ def make_inputs(w: Workload, with_dout: bool | None = None) -> dict:
     else:  # pragma: no cover
         raise ValueError(w.lens_kind)
     return {"q": q, "k": k, "v": v, "do": do, "kv_lens": lens}
+
+
+def make_paged(k, v, seq_lens, page_size: int, seed: int, spare_pages: int = 2):
+    """Scatter dense K/V [B, S, Hkv, D] into shuffled page pools, as a paged cache holds them.
+
+    Returns ``(k_pages, v_pages, block_table, max_pages)``: pools [num_pages, page_size,
+    Hkv, D] in the dtype of ``k``; block_table int32 [B, max_pages] with max_pages =
+    ceil(S / page_size). Only the pages that hold valid keys (t < seq_lens[b]) are
+    assigned, to pages in a seeded random order; every other pool row (the tail of a
+    partly filled page, unassigned and spare pages) holds NaN, and unassigned table
+    entries hold -1, so that anything read past a valid length shows up.
+    """
+    B, S, Hkv, D = k.shape
+    max_pages = -(-S // page_size)
+    lens = [int(x) for x in seq_lens]
+    need = [-(-L // page_size) for L in lens]
+    num_pages = sum(need) + spare_pages
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    order = torch.randperm(num_pages, generator=g).tolist()
+    kp = torch.full((num_pages, page_size, Hkv, D), float("nan"), dtype=k.dtype)
+    vp = torch.full((num_pages, page_size, Hkv, D), float("nan"), dtype=v.dtype)
+    bt = torch.full((B, max_pages), -1, dtype=torch.int32)
+    used = 0
+    for b in range(B):
+        for t in range(need[b]):
+            page = order[used]
+            used += 1
+            bt[b, t] = page
+            n = min(page_size, lens[b] - t * page_size)
+            kp[page, :n] = k[b, t * page_size:t * page_size + n]
+            vp[page, :n] = v[b, t * page_size:t * page_size + n]
+    return kp.contiguous(), vp.contiguous(), bt.contiguous(), max_pages

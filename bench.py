@@ -42,6 +42,7 @@ from attention_sm_flash_gb300 import metrics, workloads  # noqa: E402
 
 METRIC = "attention fwd/bwd TFLOP/s (bf16) and % of GB300 dense BF16 tensor peak"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+DEFAULT_ALSO = "c3,c4v,c5,c4@paged256,dec1@dense,dec1@split,sq64@dense,sq64@split"
 # FP32 FMA peak for the CUDA-core path: 152 SMs x 128 FMA/clk x 2 FLOP x 2.07 GHz
 FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 
@@ -52,9 +53,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="c4", choices=sorted(workloads.WORKLOADS))
-    ap.add_argument("--also", default="c3,c4v,c5",
+    ap.add_argument("--also", default=DEFAULT_ALSO,
                     help="comma-separated workloads timed after the headline one, in the "
-                         "same process (empty: none)")
+                         "same process, each as key[@mode] with mode dense (default), split "
+                         "(attn_fwd_splitkv) or pagedN (attn_fwd_paged, N-key pages); empty: "
+                         "none")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work in the oracle baseline sample")
@@ -265,19 +268,43 @@ def traffic_for(kernel_key):
     return None
 
 
+def fwd_bytes(w, lens) -> float:
+    """Algorithmic HBM bytes of one forward: Q read and O written once, LSE written, and
+    the valid rows of K and V read once."""
+    el = 2 if w.dtype == "bf16" else 4
+    valid = (w.B * w.Hkv * w.Skv if lens is None else int(lens.to(torch.int64).sum()))
+    return 2.0 * w.B * w.Sq * w.Hq * w.D * el + 4.0 * w.B * w.Hq * w.Sq + 2.0 * valid * w.D * el
+
+
 class Workbench:
     """One workload's device buffers and its timed step (attn_fwd, then attn_bwd where the
-    workload has a backward) on one stream, L2 flushed before every step."""
+    workload has a backward) on one stream, L2 flushed before every step. ``mode``: dense
+    (attn_fwd), split (attn_fwd_splitkv) or pagedN (attn_fwd_paged over shuffled N-key
+    pages holding the same keys)."""
 
-    def __init__(self, w, inp, dev, stream, flush_buf):
+    def __init__(self, w, inp, dev, stream, flush_buf, mode="dense"):
         from attention_sm_flash_gb300 import attn
 
         self.attn, self.w, self.inp, self.stream, self.flush_buf = attn, w, inp, stream, flush_buf
-        self.q, self.k, self.v = (inp[n].to(dev) for n in ("q", "k", "v"))
+        self.mode = mode
+        self.q = inp["q"].to(dev)
         self.do = inp["do"].to(dev) if w.has_bwd else None
         self.lens = inp["kv_lens"].to(dev) if inp["kv_lens"] is not None else None
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+        if mode.startswith("paged"):
+            ps = int(mode[len("paged"):])
+            lens = ([w.Skv] * w.B if inp["kv_lens"] is None else
+                    [int(x) for x in inp["kv_lens"][:, 0]])
+            kp, vp, bt, _ = workloads.make_paged(inp["k"], inp["v"], lens, ps, seed=w.seed)
+            self.k, self.v, self.bt = kp.to(dev), vp.to(dev), bt.to(dev)
+            self.seq = torch.tensor(lens, dtype=torch.int32, device=dev)
+        else:
+            self.k, self.v = inp["k"].to(dev), inp["v"].to(dev)
+        if mode == "split":
+            need = attn.attn_fwd_splitkv_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D,
+                                                        attn.ATTN_BF16)
+            self.fws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
         if w.has_bwd:
             self.dq, self.dk, self.dv = (torch.empty_like(t) for t in (self.q, self.k, self.v))
             code = attn.ATTN_BF16 if w.dtype == "bf16" else attn.ATTN_F32
@@ -286,8 +313,15 @@ class Workbench:
 
     def fwd(self):
         w = self.w
-        self.attn.attn_fwd(self.q, self.k, self.v, self.o, self.lse, w.causal, w.scale,
-                           self.lens, self.stream)
+        if self.mode == "split":
+            self.attn.attn_fwd_splitkv(self.q, self.k, self.v, self.o, self.lse, w.causal,
+                                       w.scale, self.lens, self.fws, self.stream)
+        elif self.mode.startswith("paged"):
+            self.attn.attn_fwd_paged(self.q, self.k, self.v, self.bt, self.seq, self.o,
+                                     self.lse, w.causal, w.scale, self.stream)
+        else:
+            self.attn.attn_fwd(self.q, self.k, self.v, self.o, self.lse, w.causal, w.scale,
+                               self.lens, self.stream)
 
     def bwd(self):
         w = self.w
@@ -351,7 +385,12 @@ def also_entry(bench, args, world, sampler_index, peaks, peak_src, dev):
     bm = reduce_max(statistics.mean(bwd_ms), dev) if w.has_bwd else 0.0
     peak, bound, note = tensor_peak(w, peaks, peak_src)
     fwd_t = whole_job_tflops(fwd_fl, fm, world)
+    gbs = world * fwd_bytes(w, bench.inp["kv_lens"]) / (fm * 1e-3) / 1e9
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    call = {"dense": "attn_fwd", "split": "attn_fwd_splitkv"}.get(bench.mode, "attn_fwd_paged")
     out = {"workload": cfg["workload"], "Skv_eff": cfg["Skv_eff"], "step": cfg["step"],
+           "forward_call": call,
+           "fwd_gbs": round(gbs, 1), "fwd_hbm_frac": round(gbs / world / hbm, 4),
            "value": round(whole_job_tflops(fwd_fl + bwd_fl, fm + bm, world), 3),
            "ms_per_step": round(fm + bm, 5), "fwd_ms": round(fm, 5),
            "fwd_tflops": round(fwd_t, 3), "fwd_frac": round(fwd_t / world / peak, 4),
@@ -362,7 +401,7 @@ def also_entry(bench, args, world, sampler_index, peaks, peak_src, dev):
         out.update({"bwd_ms": round(bm, 5), "bwd_tflops": round(bwd_t, 3),
                     "bwd_frac": round(bwd_t / world / peak, 4),
                     "bwd_traffic": traffic_for(f"attn_bwd:{w.key}")})
-    if w.key != "c3":
+    if w.key != "c3" and bench.mode == "dense":
         out["fwd_traffic"] = traffic_for(f"attn_fwd:{w.key}")
     return out
 
@@ -476,10 +515,11 @@ def run_ours(args, rank, world, local_rank):
     # the other graded workloads, timed the same way in the same process
     del bench, q, k, v, do, lens, o, lse
     also = {}
-    for key in [x for x in args.also.split(",") if x and x != w.key]:
+    for entry in [x for x in args.also.split(",") if x and x != w.key]:
+        key, _, mode = entry.partition("@")
         wa = workloads.get(key)
-        ba = Workbench(wa, workloads.make_inputs(wa), dev, stream, flush_buf)
-        also[key] = also_entry(ba, args, world, sampler_index, peaks, peak_src, dev)
+        ba = Workbench(wa, workloads.make_inputs(wa), dev, stream, flush_buf, mode or "dense")
+        also[entry] = also_entry(ba, args, world, sampler_index, peaks, peak_src, dev)
         del ba
         torch.cuda.empty_cache()
     if also:

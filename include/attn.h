@@ -84,6 +84,9 @@ typedef enum {
 #define ATTN_DEVERR_LAYOUT 0x4u  /* a kernel's shared memory was not 1024-byte aligned, which
                                     its swizzled tiles need; it computed nothing, outputs are
                                     invalid */
+#define ATTN_DEVERR_PAGE 0x8u    /* a block-table entry that a paged forward needed was not a
+                                    page of the pool; page 0 was read instead, outputs are
+                                    invalid */
 
 /*
  * Forward. q, k, v: inputs; o: output [B, Sq, Hq, D]; lse: output [B, Hq, Sq] fp32.
@@ -111,6 +114,66 @@ ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, con
                        int B, int Hq, int Hkv, int Sq, int Skv, int D, float scale,
                        int causal, const int32_t* kv_lens, attn_dtype_t dtype,
                        void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * Paged forward: attention over a K/V cache kept in fixed-size pages, read through a
+ * per-sequence block table instead of first gathering the pages into contiguous K/V
+ * ("LingBot full-pipeline analysis report", section "optimisation migration matrix v2",
+ * row H1a_kv_gather_off: direct paged FA through the block table against gather + FA
+ * varlen; the self-attention cache keeps a block table and per-sequence lengths,
+ * section "layer-0 internal diagnosis v5").
+ *     q, o             : [B, Sq, Hq, D] bf16
+ *     k_pages, v_pages : [num_pages, page_size, Hkv, D] bf16, the key and value pools
+ *     block_table      : [B, max_pages] int32, device memory: entry t of sequence b is the
+ *                        page that holds its keys t * page_size .. (t + 1) * page_size - 1;
+ *                        only entries of pages that hold valid keys are read
+ *     seq_lens         : [B] int32, device memory: valid keys of each sequence, shared by
+ *                        its kv heads; NULL = max_pages * page_size for every sequence
+ *     lse              : [B, Hq, Sq] fp32
+ * The result is attn_fwd on the gathered K/V [B, max_pages * page_size, Hkv, D] with
+ * kv_lens[b][kvh] = seq_lens[b]: the same GQA, causal (bottom-right) and empty-row rules.
+ * page_size must be a power of two of at least 16, num_pages and max_pages >= 1, dtype
+ * ATTN_BF16 (else ATTN_ERR_UNSUPPORTED; the other checks are those of attn_fwd). A
+ * seq_lens entry outside [0, max_pages * page_size] is clamped and flagged
+ * (ATTN_DEVERR_KVLEN); a needed block-table entry outside [0, num_pages) is flagged
+ * (ATTN_DEVERR_PAGE) and page 0 is read in its place. Pointers: q, k_pages, v_pages, o
+ * 16-byte aligned; block_table, seq_lens, lse 4-byte aligned.
+ */
+ATTN_API attn_status_t attn_fwd_paged(const void* q, const void* k_pages, const void* v_pages,
+                                      const int32_t* block_table, const int32_t* seq_lens,
+                                      void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+                                      int num_pages, int page_size, int max_pages, int D,
+                                      float scale, int causal, attn_dtype_t dtype,
+                                      attn_stream_t stream);
+
+/*
+ * Split-KV forward, for short query blocks over long K/V: single-query decode ("xtrain
+ * evolution.md", phase-3 milestone M2a: decode attention equals the last causal row of
+ * the full computation) and a few query rows against a whole cache, where the per-rank
+ * work is too short to fill the GPU (LingBot report, section "Attention effective-FLOP
+ * utilisation curve (A0)": utilisation falls as the per-call work shrinks). Arguments,
+ * layout, results and errors are those of attn_fwd, plus a workspace of
+ * attn_fwd_splitkv_workspace_size() bytes of device memory (256-byte aligned, for the
+ * call's exclusive use until the stream reaches its end; ATTN_ERR_WORKSPACE otherwise).
+ * Each (batch, head, 128-row query block) is cut into ranges of key tiles processed as
+ * separate work items; an item writes its normalised partial O and LSE (fp32) to the
+ * workspace and a second kernel merges a row's ranges in range order (deterministic):
+ * lse = log(sum_s exp(lse_s)), O = sum_s exp(lse_s - lse) O_s. When the problem already
+ * has enough work items the call is exactly attn_fwd and the workspace is not touched.
+ */
+ATTN_API attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o,
+                                        float* lse, int B, int Hq, int Hkv, int Sq, int Skv,
+                                        int D, float scale, int causal, const int32_t* kv_lens,
+                                        attn_dtype_t dtype, void* workspace,
+                                        size_t workspace_bytes, attn_stream_t stream);
+
+/* Bytes of device workspace attn_fwd_splitkv needs for these sizes: 0 when it does not
+ * split (fp32, or enough (batch, head, query block) items: at least 152), else
+ * n * B * Hq * Sq * (D + 1) * 4 bytes (each rounded up to 256) for n key ranges per item,
+ * n = ceil(304 / items) capped so that each range holds at least 4 tiles of 128 keys.
+ * A pure function of the sizes. */
+ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                                                attn_dtype_t dtype);
 
 /* Bytes of device workspace attn_bwd needs for these sizes (0 for an empty problem):
  * delta [B, Hq, Sq] fp32, plus, for bf16 GQA problems with fewer than 256 (batch, kv
@@ -167,8 +230,8 @@ ATTN_API attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void
  * Waits for `stream`, then reads and clears the current device's error word.
  * Writes the raw ATTN_DEVERR_* bits to *bits when bits is not NULL. Returns
  * ATTN_ERR_TIMEOUT if the timeout bit was set, else ATTN_ERR_CUDA if the layout bit was
- * set, ATTN_ERR_INVALID_ARG if only the kv_lens bit was set, ATTN_OK if the word was
- * clear, ATTN_ERR_CUDA on a CUDA error.
+ * set, ATTN_ERR_INVALID_ARG if only the kv_lens or page bit was set, ATTN_OK if the word
+ * was clear, ATTN_ERR_CUDA on a CUDA error.
  */
 ATTN_API attn_status_t attn_peek_device_error(uint32_t* bits, attn_stream_t stream);
 

@@ -202,3 +202,69 @@ def test_binding_checks_shapes_and_dtypes_bwd(bad):
     with pytest.raises(ValueError):
         attn.attn_bwd_noalloc(t["q"], t["k"], t["v"], t["o"], t["dout"], lse, t["dq"], t["dk"],
                               t["dv"])
+
+
+def paged(lib, **kw):
+    args = dict(q=A, kp=A, vp=A, bt=A, lens=A, o=A, lse=A, B=2, Hq=4, Hkv=2, Sq=8, pages=6,
+                page_size=128, max_pages=3, D=128, scale=0.088, causal=0,
+                dtype=attn.ATTN_BF16, stream=None)
+    args.update(kw)
+    return lib.attn_fwd_paged(*args.values())
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(page_size=48), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(page_size=8), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(page_size=200), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(page_size=384), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=attn.ATTN_F32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(D=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(pages=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(max_pages=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(page_size=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(max_pages=1 << 24, page_size=1 << 10), attn.ATTN_ERR_INVALID_ARG),
+    (dict(bt=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(kp=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(bt=A + 2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(lens=A + 1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(vp=A + 8), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+])
+def test_paged_rejects_bad_arguments(lib, kw, want):
+    assert paged(lib, **kw) == want
+
+
+def test_paged_empty_problem_is_a_no_op(lib):
+    assert paged(lib, B=0) == attn.ATTN_OK
+    assert paged(lib, Sq=0, q=None, o=None) == attn.ATTN_OK
+
+
+def test_splitkv_workspace_size(lib):
+    f = attn.attn_fwd_splitkv_workspace_size
+    # decode over the DiT cache: 40 (batch, head) items -> 8 ranges of 32 key tiles
+    assert f(1, 40, 40, 1, 32760, 128, attn.ATTN_BF16) == (8 * 40 * 128 * 4) + 256 * 5
+    # 64 query rows: still one query block per head
+    assert f(1, 40, 40, 64, 32760, 128, attn.ATTN_BF16) == 8 * 40 * 64 * 128 * 4 + 8 * 40 * 64 * 4
+    # one head, short K/V: at least 4 tiles per range (9 tiles -> 2 ranges)
+    assert f(1, 1, 1, 1, 9 * 128, 64, attn.ATTN_BF16) == 2 * 64 * 4 + 256
+    # enough items without splitting, fp32, tiny K/V, empty problems: no workspace
+    assert f(1, 40, 40, 32760, 32760, 128, attn.ATTN_BF16) == 0
+    assert f(1, 40, 40, 1, 32760, 128, attn.ATTN_F32) == 0
+    assert f(1, 1, 1, 1, 300, 128, attn.ATTN_BF16) == 0
+    assert f(0, 40, 40, 1, 32760, 128, attn.ATTN_BF16) == 0
+
+
+def test_splitkv_needs_its_workspace(lib):
+    def call(**kw):
+        args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, Hq=40, Hkv=40, Sq=1, Skv=32760, D=128,
+                    scale=0.088, causal=0, lens=None, dtype=attn.ATTN_BF16, ws=A,
+                    ws_bytes=1 << 20, stream=None)
+        args.update(kw)
+        return lib.attn_fwd_splitkv(*args.values())
+    assert call(ws=None) == attn.ATTN_ERR_WORKSPACE
+    assert call(ws_bytes=1000) == attn.ATTN_ERR_WORKSPACE
+    assert call(ws=A + 64) == attn.ATTN_ERR_WORKSPACE
+    assert call(D=80) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(q=A + 4) == attn.ATTN_ERR_INVALID_ARG
+    assert call(B=0) == attn.ATTN_OK
