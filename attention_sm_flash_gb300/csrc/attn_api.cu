@@ -94,7 +94,7 @@ extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, v
   cudaError_t e = error_word(&p.err);
   if (e != cudaSuccess) return from_cuda(e);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return from_cuda(dtype == ATTN_BF16 ? tc_fwd(p, s) : simt_fwd(p, s));
+  return from_cuda(dtype == ATTN_BF16 ? tc_fwd(p, s) : tf32_fwd(p, s));
 }
 
 extern "C" attn_status_t attn_fwd_paged(const void* q, const void* k_pages,
@@ -273,5 +273,5 @@ extern "C" uint64_t attn_launch_count(void) { return g_launches.load(std::memory
 
 extern "C" const char* attn_build_info(void) {
   return "libattn sm_103a: bf16 fwd (dense, paged, split-KV) + bwd tcgen05/TMA/TMEM; fp32 "
-         "fwd/bwd CUDA-core";
+         "fwd tcgen05 3xTF32, fp32 bwd CUDA-core";
 }

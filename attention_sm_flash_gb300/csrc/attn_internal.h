@@ -98,8 +98,7 @@ inline size_t bwd_partial_bytes(int B, int Hkv, int parts, int Skv, int D) {
 // Counts one kernel launch issued by the library (see attn_launch_count()).
 void count_launches(int n);
 
-// CUDA-core kernels (fp32 arithmetic): the fp32 path, any D in {64, 128}.
-cudaError_t simt_fwd(const Problem& p, cudaStream_t stream);
+// CUDA-core kernels (fp32 arithmetic): the fp32 backward, any D in {64, 128}.
 cudaError_t simt_bwd(const Problem& p, cudaStream_t stream);
 // delta = rowsum(dO * O) into p.delta (one warp per row), for the CUDA-core backward
 // (the bf16 backward has a delta kernel of its own).
@@ -108,6 +107,8 @@ cudaError_t simt_delta(const Problem& p, cudaStream_t stream);
 // Tensor-core (tcgen05) kernels for bf16, sm_103a. tc_fwd covers the dense, the paged
 // and the split-KV forward (the latter adds the merge kernel).
 cudaError_t tc_fwd(const Problem& p, cudaStream_t stream);
+// The fp32 forward on the tensor cores (tcgen05 kind::tf32, three-term split).
+cudaError_t tf32_fwd(const Problem& p, cudaStream_t stream);
 cudaError_t tc_bwd(const Problem& p, cudaStream_t stream);
 
 // A bf16 [B, S, H, D] tensor as a 4-D TMA map (D, H, S, B) whose box is one head:

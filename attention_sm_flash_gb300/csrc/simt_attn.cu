@@ -1,14 +1,10 @@
-// CUDA-core attention kernels with fp32 arithmetic (FFMA + expf), forward and backward.
+// CUDA-core attention backward with fp32 arithmetic (FFMA + expf): the fp32 element-type
+// path of attn_bwd, which must meet a 1e-5 relative tolerance (the fp32 forward runs on
+// the tensor cores with a three-term TF32 split, fwd_tf32x3.cu).
 //
-// This is the fp32 element-type path: fp32 inputs must meet a 1e-5 relative tolerance,
-// which rules out TF32 tensor cores, so the contraction runs on the FMA pipe.
-//
-// Forward: the online softmax over K/V tiles ("xtrain evolution.md", infra table row
-// T14): per query row a running max m and sum l; each K/V tile of BN keys is scored,
-// the row's accumulator is rescaled by exp(m_old - m_new) and the tile's weights
-// exp(s - m_new) are added. Backward (same row): recompute the scores from Q, K and
-// LSE, delta = rowsum(dO * O), dS = P * (dP - delta); a dK/dV kernel owns its key rows
-// and loops over the query heads of the GQA group (row T15: in-group sum in a fixed
+// Backward ("xtrain evolution.md", infra table row T14): recompute the scores from Q, K
+// and LSE, delta = rowsum(dO * O), dS = P * (dP - delta); a dK/dV kernel owns its key
+// rows and loops over the query heads of the GQA group (row T15: in-group sum in a fixed
 // order, no atomics), and a dQ kernel owns its query rows. All sums run in a fixed
 // order, so results are bitwise reproducible.
 //
@@ -52,77 +48,6 @@ __device__ __forceinline__ void load_tile(float (*dst)[D], const T* base, int64_
     const int row = r0 + r;
     dst[r][d] = row < valid ? to_f32(base[(int64_t)row * row_stride + d]) : 0.f;
   }
-}
-
-template <typename T, int D>
-__global__ void __launch_bounds__(kRows * kTpr)
-simt_fwd_kernel(Problem p) {
-  constexpr int DPT = D / kTpr;
-  __shared__ float sK[kTile][D];
-  __shared__ float sV[kTile][D];
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int g = p.Hq / p.Hkv, kvh = h / g;
-  const int L = load_kv_len(p.kv_lens, b, kvh, p.Hkv, p.Skv, threadIdx.x == 0 ? p.err : nullptr);
-  const int r = threadIdx.x / kTpr, t = threadIdx.x % kTpr;
-  const int i0 = blockIdx.x * kRows;
-  const int i = i0 + r;
-  const bool row_ok = i < p.Sq;
-  const T* Q = static_cast<const T*>(p.q);
-  const T* K = static_cast<const T*>(p.k) + ((int64_t)b * p.Skv * p.Hkv + kvh) * D;
-  const T* V = static_cast<const T*>(p.v) + ((int64_t)b * p.Skv * p.Hkv + kvh) * D;
-  const int64_t kv_stride = (int64_t)p.Hkv * D;
-  const int64_t qoff = (((int64_t)b * p.Sq + i) * p.Hq + h) * D;
-
-  float qr[DPT], acc[DPT];
-#pragma unroll
-  for (int c = 0; c < DPT; ++c) {
-    qr[c] = row_ok ? to_f32(Q[qoff + kTpr * c + t]) : 0.f;
-    acc[c] = 0.f;
-  }
-  // keys visible to some row of this block: j < L and (causal) j <= i_last + L - Sq
-  int kend = L;
-  if (p.causal) kend = min(L, max(0, i0 + kRows - 1 + L - p.Sq + 1));
-  float m = -CUDART_INF_F, l = 0.f;
-  for (int j0 = 0; j0 < kend; j0 += kTile) {
-    __syncthreads();
-    load_tile<T, D>(sK, K, kv_stride, j0, L);
-    load_tile<T, D>(sV, V, kv_stride, j0, L);
-    __syncthreads();
-    float s[kTile];
-    float mt = -CUDART_INF_F;
-#pragma unroll
-    for (int jj = 0; jj < kTile; ++jj) {
-      float part = 0.f;
-#pragma unroll
-      for (int c = 0; c < DPT; ++c) part = fmaf(qr[c], sK[jj][kTpr * c + t], part);
-      part = row_sum4(part);
-      const int j = j0 + jj;
-      const bool vis = row_ok && j < L && (!p.causal || j <= i + L - p.Sq);
-      s[jj] = vis ? part * p.scale : -CUDART_INF_F;
-      mt = fmaxf(mt, s[jj]);
-    }
-    const float mn = fmaxf(m, mt);
-    if (mn == -CUDART_INF_F) continue;  // nothing visible to this row yet
-    const float alpha = expf(m - mn);   // exp(-inf) = 0 on the first visible tile
-    l *= alpha;
-#pragma unroll
-    for (int c = 0; c < DPT; ++c) acc[c] *= alpha;
-#pragma unroll
-    for (int jj = 0; jj < kTile; ++jj) {
-      const float pj = expf(s[jj] - mn);
-      l += pj;
-#pragma unroll
-      for (int c = 0; c < DPT; ++c) acc[c] = fmaf(pj, sV[jj][kTpr * c + t], acc[c]);
-    }
-    m = mn;
-  }
-  if (!row_ok) return;
-  T* O = static_cast<T*>(p.o);
-  const bool any = l > 0.f;
-  const float inv = any ? 1.f / l : 0.f;
-#pragma unroll
-  for (int c = 0; c < DPT; ++c) O[qoff + kTpr * c + t] = from_f32<T>(acc[c] * inv);
-  if (t == 0) p.lse[((int64_t)b * p.Hq + h) * p.Sq + i] = any ? m + logf(l) : -CUDART_INF_F;
 }
 
 // delta[b, h, i] = sum_d dO[b, i, h, d] * O[b, i, h, d]; one warp per row.
@@ -296,14 +221,6 @@ simt_dq_kernel(Problem p) {
 }
 
 template <typename T, int D>
-cudaError_t fwd_launch(const Problem& p, cudaStream_t s) {
-  dim3 grid((p.Sq + kRows - 1) / kRows, p.Hq, p.B);
-  simt_fwd_kernel<T, D><<<grid, kRows * kTpr, 0, s>>>(p);
-  count_launches(1);
-  return cudaGetLastError();
-}
-
-template <typename T, int D>
 cudaError_t bwd_launch(const Problem& p, cudaStream_t s) {
   const int64_t rows = (int64_t)p.B * p.Sq * p.Hq;
   simt_delta_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p);
@@ -336,11 +253,6 @@ cudaError_t delta_launch(const Problem& p, cudaStream_t s) {
 cudaError_t simt_delta(const Problem& p, cudaStream_t s) {
   if (p.dtype == ATTN_F32) return p.D == 64 ? delta_launch<float, 64>(p, s) : delta_launch<float, 128>(p, s);
   return p.D == 64 ? delta_launch<__nv_bfloat16, 64>(p, s) : delta_launch<__nv_bfloat16, 128>(p, s);
-}
-
-cudaError_t simt_fwd(const Problem& p, cudaStream_t s) {
-  if (p.dtype == ATTN_F32) return p.D == 64 ? fwd_launch<float, 64>(p, s) : fwd_launch<float, 128>(p, s);
-  return p.D == 64 ? fwd_launch<__nv_bfloat16, 64>(p, s) : fwd_launch<__nv_bfloat16, 128>(p, s);
 }
 
 cudaError_t simt_bwd(const Problem& p, cudaStream_t s) {

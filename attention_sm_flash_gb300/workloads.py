@@ -18,7 +18,9 @@ available here), with the pages' shapes:
   (the report's varlen FA3 path with cu_seqlens shorter than the allocation, section
   "same-GPU FA2/FA3 hardware comparison");
 * ``c5``  video-DiT cross-attention: Sq 32760 video tokens, Skv 512 text tokens of which
-  300 are valid (section "recorded cross-attention matrix work": K = 512 text tokens).
+  300 are valid (section "recorded cross-attention matrix work": K = 512 text tokens);
+* ``vae_f32`` fp32 attention over one 60 x 104 latent frame (the report's fp32 VAE frame
+  attention, fmha_cutlassF_f32), 8 heads of 128 (not stated on the pages).
 
 Recipe: a CPU ``torch.Generator`` seeded with 20260 + the config number draws fp32
 standard normals in the order Q, K, V, dO (dO only where the workload has a backward);
@@ -90,6 +92,12 @@ WORKLOADS = {
     # a 28080-token KV cache, 40 heads): context for its FA3 figure, not a graded workload
     "ctx": Workload("ctx", "page_dit_self_q4680_k28080_h40_d128", 1, 40, 40, 4680, 28080, 128,
                     "bf16", False, 20268, qk_factor=0.5),
+    # fp32 attention over one latent frame of the 480 x 832 video (60 x 104 = 6240
+    # tokens), the role of the report's VAE frame attention (fmha_cutlassF_f32 in
+    # vae_frame); the report gives neither its head count nor its head dimension, so 8
+    # heads of 128 stand in
+    "vae_f32": Workload("vae_f32", "vae_frame_f32_b1_h8_s6240_d128", 1, 8, 8, 6240, 6240, 128,
+                        "f32", False, 20271),
     # short query blocks over the DiT self-attention's K/V cache (32760 tokens, 40 heads):
     # single-query decode (causal, bottom-right: the query sees every key, the last causal
     # row of xtrain's decode milestone) and 64 query rows; the split-KV forward's cases

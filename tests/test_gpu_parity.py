@@ -76,7 +76,7 @@ def sample_rows(Sq, n, seed):
     return np.unique(np.concatenate([fixed, extra])).astype(np.int64)
 
 
-@pytest.mark.parametrize("key", ["c4", "c4v", "c5"])
+@pytest.mark.parametrize("key", ["c4", "c4v", "c5", "vae_f32"])
 def test_dit_workloads_sampled_rows(key):
     w = workloads.get(key)
     inp = workloads.make_inputs(w)
