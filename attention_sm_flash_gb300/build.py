@@ -56,19 +56,34 @@ def _stamp(extra_flags) -> str:
     return h.hexdigest()
 
 
-def source_digest() -> str:
+def source_digest(kernel_files=None) -> str:
     """Hash of the CUDA sources and headers by relative path and content only (the same on
     any machine and checkout path): the key under which measured per-kernel figures, such
-    as DRAM traffic, are recorded."""
+    as DRAM traffic, are recorded. ``kernel_files``: names of the .cu files that hold the
+    measured kernels (with every header, the code they include); None = all sources."""
     h = hashlib.sha256()
-    files = _sources() + sorted(glob.glob(os.path.join(CSRC, "*.h")) +
-                                glob.glob(os.path.join(CSRC, "*.cuh")) +
-                                glob.glob(os.path.join(ROOT, "include", "*.h")))
+    sources = _sources()
+    if kernel_files is not None:
+        sources = [f for f in sources if os.path.basename(f) in set(kernel_files)]
+    files = sources + sorted(glob.glob(os.path.join(CSRC, "*.h")) +
+                             glob.glob(os.path.join(CSRC, "*.cuh")) +
+                             glob.glob(os.path.join(ROOT, "include", "*.h")))
     for f in sorted(files, key=lambda p: os.path.relpath(p, ROOT)):
         h.update(os.path.relpath(f, ROOT).encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+# the source file of each operation's kernels by element type, for per-kernel digests
+OP_SOURCES = {
+    ("attn_fwd", "bf16"): ["fwd_sm103.cu"],
+    ("attn_fwd", "f32"): ["fwd_tf32x3.cu"],
+    ("attn_fwd_paged", "bf16"): ["fwd_sm103.cu"],
+    ("attn_fwd_splitkv", "bf16"): ["fwd_sm103.cu"],
+    ("attn_bwd", "bf16"): ["bwd_sm103.cu"],
+    ("attn_bwd", "f32"): ["simt_attn.cu"],
+}
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:

@@ -253,13 +253,15 @@ def whole_job_tflops(flops_per_rank_step: float, ms_max: float, world: int) -> f
 
 
 # --------------------------------------------------------------------------- ours
-def traffic_for(kernel_key):
-    """DRAM bytes per launch recorded from an ncu capture of the current sources, or None."""
+def traffic_for(kernel_key, dtype="bf16"):
+    """DRAM bytes per call recorded from an ncu capture of the current sources of that
+    operation's kernels, or None (no record, or the kernels changed since)."""
     path = os.path.join(HERE, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
     from attention_sm_flash_gb300 import build as libbuild
-    stamp = libbuild.source_digest()
+    op = kernel_key.split(":")[0]
+    stamp = libbuild.source_digest(libbuild.OP_SOURCES.get((op, dtype)))
     with open(path) as f:
         for line in f:
             parts = line.split()
@@ -403,9 +405,10 @@ def also_entry(bench, args, world, sampler_index, peaks, peak_src, dev):
         bwd_t = whole_job_tflops(bwd_fl, bm, world)
         out.update({"bwd_ms": round(bm, 5), "bwd_tflops": round(bwd_t, 3),
                     "bwd_frac": round(bwd_t / world / peak, 4),
-                    "bwd_traffic": traffic_for(f"attn_bwd:{w.key}")})
-    if w.key != "c3" and bench.mode == "dense":
-        out["fwd_traffic"] = traffic_for(f"attn_fwd:{w.key}")
+                    "bwd_traffic": traffic_for(f"attn_bwd:{w.key}", w.dtype)})
+    if w.key != "c3":
+        op = {"dense": "attn_fwd", "split": "attn_fwd_splitkv"}.get(bench.mode, "attn_fwd_paged")
+        out["fwd_traffic"] = traffic_for(f"{op}:{w.key}", w.dtype)
     return out
 
 
@@ -492,7 +495,7 @@ def run_ours(args, rank, world, local_rank):
                "attn_bwd": "bwd_delta + bwd_dq + bwd_dkdv (+ group reduce) kernels of one call"}
     roofline = {"bound": bound, "achieved": round(achieved, 3), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "traffic": traffic_for(f"{dom}:{w.key}"), "kernel": kernels[dom],
+                "traffic": traffic_for(f"{dom}:{w.key}", w.dtype), "kernel": kernels[dom],
                 "call": dom, "peak_source": peak_note,
                 "algorithmic_flops_per_launch": dom_fl}
     bf16_peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
