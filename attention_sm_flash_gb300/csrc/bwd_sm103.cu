@@ -564,7 +564,11 @@ struct DkvCtl {
   // a stage's Q and dO are released separately: dO once dP^T and dV have read it (two
   // commits, one per issuer), Q once dK has, later in the tile
   uint64_t q_full[NST], q_empty[NST], do_full[NST], do_empty[NST];
-  uint64_t s_full, s_free, dp_full, p_ready, ds_ready, dv_done, dk_done;
+  uint64_t s_full, s_free, p_ready, dv_done;
+  // per dP^T buffer: dP^T landed / dK has read the dS^T written there. With two buffers
+  // dP^T may run two tiles ahead of the elementwise warps, and a parity wait only tells
+  // apart phases one apart, so each buffer has its own barrier.
+  uint64_t dp_full[2], ds_ready[2], dk_done[2];
   uint64_t acc_done, acc_free, mma_final, mma_final2;
   uint32_t tmem_base;
   int abort;
@@ -664,11 +668,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
     }
     mbar_init(&c.s_full, 1);
     mbar_init(&c.s_free, kEwWarps);
-    mbar_init(&c.dp_full, 1);
+    mbar_init(&c.dp_full[0], 1);
+    mbar_init(&c.dp_full[1], 1);
     mbar_init(&c.p_ready, kEwWarps);
-    mbar_init(&c.ds_ready, kEwWarps);
+    mbar_init(&c.ds_ready[0], kEwWarps);
+    mbar_init(&c.ds_ready[1], kEwWarps);
     mbar_init(&c.dv_done, 1);
-    mbar_init(&c.dk_done, 1);
+    mbar_init(&c.dk_done[0], 1);
+    mbar_init(&c.dk_done[1], 1);
     mbar_init(&c.acc_done, 1);
     mbar_init(&c.acc_free, kEwWarps);
     mbar_init(&c.mma_final, 1);
@@ -687,7 +694,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
   // P^T goes to shared memory (dV += P^T dO reads both operands there), so S^T(g + 1) may
   // be issued as soon as the elementwise warps hold S^T(g) in registers.
   const uint32_t tmem = c.tmem_base;
-  const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + D;
+  // With D = 64 there is room for a second dP^T buffer [256, 384) (dV and dK move up):
+  // dP^T(g + 1) then need not wait for dK(g) to read dS^T(g), which breaks the chain
+  // dK(g) -> dP^T(g + 1) -> dS^T(g + 1) -> dK(g + 1) that sets the tile period.
+  constexpr int NDP = D == 64 ? 2 : 1;
+  const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 128 + 128 * NDP, t_dk = t_dv + D;
   WaitCtl wc{&c.abort, p.err, p.timeout_ns};
 
   if (warp == 0) {
@@ -787,15 +798,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
           if (t == it.n_tiles - 1) mma_commit(&c.k_empty);
           if (t == 0 && !wait_phase(&c.v_full, kv_cnt & 1, wc)) { ok = false; break; }
           if (!wait_phase(&c.do_full[st], st_par, wc)) { ok = false; break; }
-          if (gt >= 1 && !wait_phase(&c.dk_done, (gt - 1) & 1, wc)) { ok = false; break; }
+          // dP^T(g) goes to buffer g % NDP once dK(g - NDP) has read dS^T(g - NDP) there
+          const uint32_t u = gt % NDP;
+          if (gt >= NDP && !wait_phase(&c.dk_done[u], ((gt / NDP) - 1) & 1, wc)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * kChunk + (kk % 4) * 32;
-            mma_ss(t_dp, smem_desc_sw128(sVa + off, 16, 1024), smem_desc_sw128(sdOa + st * kTile + off, 16, 1024),
+            mma_ss(t_dp + u * 128, smem_desc_sw128(sVa + off, 16, 1024), smem_desc_sw128(sdOa + st * kTile + off, 16, 1024),
                    kIdescSP, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&c.dp_full);
+          mma_commit(&c.dp_full[u]);
           mma_commit(&c.do_empty[st]);
           if (t == it.n_tiles - 1) mma_commit(&c.v_empty);
           if (++st == NST) { st = 0; st_par ^= 1; }
@@ -833,14 +846,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
           mma_commit(&c.dv_done);
           mma_commit(&c.do_empty[st]);
           // dK += dS^T Q
-          if (!wait_phase(&c.ds_ready, gt & 1, wc)) { ok = false; break; }
+          if (!wait_phase(&c.ds_ready[gt % NDP], (gt / NDP) & 1, wc)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk) {
             const uint64_t bq = smem_desc_sw128(sQa + st * kTile + kk * 16 * 128, kChunk, 1024);
-            mma_ts(t_dk, t_dp + (kk / 4) * 64 + (kk % 4) * 8, bq, kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(t_dk, t_dp + (gt % NDP) * 128 + (kk / 4) * 64 + (kk % 4) * 8, bq, kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&c.dk_done);
+          mma_commit(&c.dk_done[gt % NDP]);
           mma_commit(&c.q_empty[st]);
           if (++st == NST) st = 0;
           ++gt;
@@ -942,9 +955,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         float4 ndv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) ndv[e] = ndg[e];
-        if (!wait_phase_warp(&c.dp_full, gt & 1, wc)) { ok = false; break; }
+        if (!wait_phase_warp(&c.dp_full[gt % NDP], (gt / NDP) & 1, wc)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tdp = t_dp + lane_off + 64 * hsel;
+        const uint32_t tdp = t_dp + (gt % NDP) * 128 + lane_off + 64 * hsel;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float4 ndn[8];
@@ -971,7 +984,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_sm103_kernel(const __gri
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive_warp(&c.ds_ready);
+        mbar_arrive_warp(&c.ds_ready[gt % NDP]);
       }
       if (!ok) break;
       // epilogue: half 0 writes dV, half 1 writes dK (times the scale); rows past the
