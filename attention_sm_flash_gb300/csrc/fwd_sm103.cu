@@ -704,6 +704,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
       // O goes out through shared memory and TMA tile stores: written straight from the
       // registers, each thread's row slice would be 16-byte stores 32 rows apart. The
       // staging tile is free once the previous item's store has read it.
+      // Warp 4 issued the previous item's store and confirms here, an item later, that it
+      // has read the tile, so no softmax warp waits for the store at the end of an item.
+      if (warp == 4 && lane == 0 && ic_s > 0) {
+        tma_store_wait_read();
+        mbar_arrive(&c.stage_free);
+      }
       if (!wait_phase_warp(&c.stage_free, (ic_s & 1) ^ 1, wc)) { ok = false; break; }
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
@@ -734,8 +740,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
 #pragma unroll
           for (int ch = 0; ch < D / 64; ++ch) tma_store_4d(&p.tm_o, sO + ch * (kBM * 128), ch * 64, it.h, it.q0, it.b);
           tma_store_commit();
-          tma_store_wait_read();
-          mbar_arrive(&c.stage_free);
         }
         __syncwarp();
       }
