@@ -46,22 +46,35 @@ inline size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 
 // Split-KV forward: into how many key ranges each (batch, head, 128-row query block) is
 // cut, and how many 128-key tiles a range holds. Short query blocks over long K/V (decode,
-// a few query rows against a whole cache) give too few work items to fill the GPU; the
-// ranges multiply them up to about 304 (two per SM of a 152-SM GB300), each range at least
-// 4 tiles long so that an item's fill and drain stay small against its work. 1: no split.
-// A pure function of the sizes, so that the workspace query and the launch agree.
+// a few query rows against a whole cache) give too few work items to fill the GPU. The
+// split chosen minimises an estimate of the time: the rounds in which the SMs of a
+// 152-SM GB300 work through the items, times an item's length in key tiles plus 3 tiles
+// of fixed cost (Q load, pipeline fill and drain, partial-output store; measured on
+// decode over a 32760-key cache, where 7, 11, 19 and 64 ranges per head took 130, 133,
+// 136 and 167 us). Rounds matter: 40 items cut 8 ways make 320 items, 2.1 rounds, the last
+// one run by 16 SMs while the rest wait; cut 7 ways, 280 items fill 2 rounds. A range
+// holds at least 4 tiles. 1: no split. A pure function of the sizes, so that the workspace query and the
+// launch agree.
 inline int fwd_split_count(int B, int Hq, int Sq, int Skv, attn_dtype_t dtype, int* tiles_per) {
   const int tiles = (Skv + 127) / 128;
   if (tiles_per != nullptr) *tiles_per = tiles;
   if (dtype != ATTN_BF16 || B <= 0 || Hq <= 0 || Sq <= 0 || Skv <= 0) return 1;
   const long long base = (long long)B * Hq * ((Sq + 127) / 128);
-  const long long target = 304;
-  if (base >= target / 2) return 1;
-  long long n = (target + base - 1) / base;
-  const long long most = tiles / 4;
-  if (n > most) n = most;
-  if (n <= 1) return 1;
-  const int per = (int)((tiles + n - 1) / n);
+  const long long sms = 152;
+  if (base >= sms) return 1;
+  // cost in half tiles: rounds * (2 * tiles per item + 6)
+  long long best_n = 1, best = (base + sms - 1) / sms * (2LL * tiles + 6);
+  for (long long n = 2; n <= tiles / 4; ++n) {
+    const long long per = (tiles + n - 1) / n;
+    if ((tiles + per - 1) / per != n) continue;  // the same ranges as a smaller n
+    const long long cost = (base * n + sms - 1) / sms * (2 * per + 6);
+    if (cost < best) {
+      best = cost;
+      best_n = n;
+    }
+  }
+  if (best_n <= 1) return 1;
+  const int per = (int)((tiles + best_n - 1) / best_n);
   if (tiles_per != nullptr) *tiles_per = per;
   return (tiles + per - 1) / per;
 }

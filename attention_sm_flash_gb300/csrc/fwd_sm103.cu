@@ -82,9 +82,10 @@ struct FwdParams {
   float* o_part;    // [n_splits, B, Hq, Sq, D]
   float* lse_part;  // [n_splits, B, Hq, Sq]
   int B, Hq, Hkv, Sq, Skv;
-  // the divisions of the work decode, as multiplies (fastdiv.h): by n_splits, B * Hq,
-  // Hq, Hkv, n_qblocks, the GQA group g = Hq / Hkv and g * n_qblocks
-  FastDiv fd_splits, fd_bh, fd_hq, fd_hkv, fd_qb, fd_g, fd_per;
+  // the divisions of the work decode, as multiplies (fastdiv.h): by the items of one
+  // key range (n_items / n_splits), B * Hq, Hq, Hkv, n_qblocks, the GQA group
+  // g = Hq / Hkv and g * n_qblocks
+  FastDiv fd_range, fd_bh, fd_hq, fd_hkv, fd_qb, fd_g, fd_per;
   int causal;
   int head_inner;    // non-causal order with the (batch, head) index innermost
   int n_qblocks;
@@ -131,9 +132,11 @@ __device__ __forceinline__ Item decode_item(int idx, const FwdParams& p, const C
   const int g = p.fd_g.d;
   int split = 0;
   if (KIND == kSplit) {
-    const int rest = p.fd_splits.div(idx);
-    split = idx - rest * p.n_splits;
-    idx = rest;
+    // the key range varies slowest: the CTAs running at the same time read the same keys
+    // of all heads, whole rows of the [B, S, H, D] cache, rather than each its own 256-byte
+    // pieces 10 KB apart (64 query rows over a 40-head, 32760-key cache: 134 -> 130 us)
+    split = p.fd_range.div(idx);
+    idx -= split * p.fd_range.d;
   }
   int b, h, qb;
   if (p.causal) {
@@ -985,7 +988,7 @@ cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
   prm.lse_part = p.lse_part;
   prm.n_items = p.B * p.Hq * prm.n_qblocks * prm.n_splits;
   const int g = p.Hq / p.Hkv;
-  prm.fd_splits = FastDiv::make(prm.n_splits);
+  prm.fd_range = FastDiv::make(p.B * p.Hq * prm.n_qblocks);
   prm.fd_bh = FastDiv::make(p.B * p.Hq);
   prm.fd_hq = FastDiv::make(p.Hq);
   prm.fd_hkv = FastDiv::make(p.Hkv);

@@ -242,10 +242,16 @@ def test_paged_empty_problem_is_a_no_op(lib):
 
 def test_splitkv_workspace_size(lib):
     f = attn.attn_fwd_splitkv_workspace_size
-    # decode over the DiT cache: 40 (batch, head) items -> 8 ranges of 32 key tiles
-    assert f(1, 40, 40, 1, 32760, 128, attn.ATTN_BF16) == (8 * 40 * 128 * 4) + 256 * 5
+
+    def r256(n):
+        return (n + 255) // 256 * 256
+    # decode over the DiT cache: 40 (batch, head) items -> 7 ranges of 37 key tiles
+    # (280 items: 2 nearly full rounds on 152 SMs; 8 ranges would give 320, 2.1 rounds)
+    assert f(1, 40, 40, 1, 32760, 128, attn.ATTN_BF16) == r256(7 * 40 * 128 * 4) + r256(7 * 40 * 4)
     # 64 query rows: still one query block per head
-    assert f(1, 40, 40, 64, 32760, 128, attn.ATTN_BF16) == 8 * 40 * 64 * 128 * 4 + 8 * 40 * 64 * 4
+    assert f(1, 40, 40, 64, 32760, 128, attn.ATTN_BF16) == r256(7 * 40 * 64 * 128 * 4) + r256(7 * 40 * 64 * 4)
+    # 16 items over 4096 keys: 8 ranges of 4 tiles (128 items, one round)
+    assert f(1, 16, 16, 1, 4096, 128, attn.ATTN_BF16) == r256(8 * 16 * 128 * 4) + r256(8 * 16 * 4)
     # one head, short K/V: at least 4 tiles per range (9 tiles -> 2 ranges)
     assert f(1, 1, 1, 1, 9 * 128, 64, attn.ATTN_BF16) == 2 * 64 * 4 + 256
     # enough items without splitting, fp32, tiny K/V, empty problems: no workspace
