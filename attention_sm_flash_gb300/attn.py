@@ -33,7 +33,8 @@ ATTN_DEVERR_PAGE = 0x8
 EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_peek_device_error",
             "attn_status_string", "attn_build_info", "attn_launch_count", "attn_bwd_noalloc",
             "attn_test_inject_fault", "attn_last_cuda_error", "attn_fwd_paged",
-            "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_size")
+            "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_size", "attn_fwd_host",
+            "attn_fwd_host_workspace_size")
 ATTN_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _lib = None
@@ -88,6 +89,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                      vp]
     lib.attn_fwd_splitkv_workspace_size.restype = sz
     lib.attn_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i, i, i]
+    lib.attn_fwd_host.restype = i
+    lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp, sz, vp]
+    lib.attn_fwd_host_workspace_size.restype = sz
+    lib.attn_fwd_host_workspace_size.argtypes = [i, i, i, i, i, i, i]
     _lib = lib
     return lib
 
@@ -247,6 +252,42 @@ def attn_fwd_splitkv(q, k, v, o, lse, causal: bool = False, scale: float | None 
                                  _ptr(workspace), workspace.numel(), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_splitkv")
+
+
+def attn_fwd_host_workspace_size(B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,
+                                 dtype_code: int) -> int:
+    return int(load().attn_fwd_host_workspace_size(B, Hq, Hkv, Sq, Skv, D, dtype_code))
+
+
+def attn_fwd_host(q, k, v, o, lse, causal: bool = False, scale: float | None = None,
+                  kv_lens=None, workspace=None, stream=None) -> None:
+    """attn_fwd on tensors in pinned host memory (q, k, v, o, lse and kv_lens CPU tensors,
+    ``pin_memory()``), with the copies to and from the GPU overlapped with the compute,
+    chunk by chunk of kv heads. ``workspace``: a uint8 device tensor of at least
+    attn_fwd_host_workspace_size() bytes on the GPU that computes (the current device);
+    allocated here (by torch) when None. Asynchronous on ``stream``: synchronise it before
+    reading o and lse."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse), ("kv_lens", kv_lens)):
+        if t is None:
+            continue
+        if t.is_cuda or not t.is_pinned():
+            raise ValueError(f"attn_fwd_host takes pinned host tensors ({name} is not one)")
+        if not t.is_contiguous():
+            raise ValueError("libattn takes contiguous tensors only")
+    _check_shapes(q, k, v, lse, kv_lens, like_q=(("o", o),))
+    B, Sq, Hq, D = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    code = _dtype_code(q)
+    need = attn_fwd_host_workspace_size(B, Hq, Hkv, Sq, Skv, D, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    st = load().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv,
+                              D, float(scale), int(bool(causal)), _ptr(kv_lens), code,
+                              _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_host")
 
 
 def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,

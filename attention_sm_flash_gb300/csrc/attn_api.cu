@@ -39,6 +39,8 @@ cudaError_t error_word(unsigned int** out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+}  // namespace
+
 // Checks shared by the forward and the backward. Returns ATTN_OK, or the error.
 attn_status_t check_common(int B, int Hq, int Hkv, int Sq, int Skv, int D, float scale,
                            int causal, const int32_t* kv_lens, attn_dtype_t dtype) {
@@ -57,13 +59,19 @@ attn_status_t check_common(int B, int Hq, int Hkv, int Sq, int Skv, int D, float
   return ATTN_OK;
 }
 
+namespace {
+
 thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+}  // namespace
 
 attn_status_t from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return ATTN_OK;
   g_last_cuda = e;
   return ATTN_ERR_CUDA;
 }
+
+namespace {
 
 std::atomic<uint64_t> g_launches{0};
 

@@ -120,6 +120,12 @@ cudaError_t simt_delta(const Problem& p, cudaStream_t stream);
 // Tensor-core (tcgen05) kernels for bf16, sm_103a. tc_fwd covers the dense, the paged
 // and the split-KV forward (the latter adds the merge kernel).
 cudaError_t tc_fwd(const Problem& p, cudaStream_t stream);
+// The size, scale, causal, dtype and kv_lens-alignment checks shared by the entry points.
+attn_status_t check_common(int B, int Hq, int Hkv, int Sq, int Skv, int D, float scale,
+                           int causal, const int32_t* kv_lens, attn_dtype_t dtype);
+// ATTN_OK for cudaSuccess; otherwise records `e` for attn_last_cuda_error() and returns
+// ATTN_ERR_CUDA.
+attn_status_t from_cuda(cudaError_t e);
 // The fp32 forward on the tensor cores (tcgen05 kind::tf32, three-term split).
 cudaError_t tf32_fwd(const Problem& p, cudaStream_t stream);
 cudaError_t tc_bwd(const Problem& p, cudaStream_t stream);

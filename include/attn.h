@@ -175,6 +175,29 @@ ATTN_API attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void
 ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int D,
                                                 attn_dtype_t dtype);
 
+/*
+ * Forward on tensors in pinned host memory: attn_fwd's operation and results (bit for
+ * bit), for callers whose activations live on the host. q, k, v, o, lse (and kv_lens,
+ * if not NULL) are host pointers in attn_fwd's layouts, page-locked (cudaHostAlloc or
+ * cudaHostRegister; other memory, including device memory, gives ATTN_ERR_INVALID_ARG).
+ * The problem is computed in chunks of about a fifth of the kv heads (with their query
+ * heads): the inputs of one chunk are copied in while the previous chunk is computed and
+ * the one before it copied out, so the link and the GPU work at the same time.
+ * `workspace`: device memory of attn_fwd_host_workspace_size() bytes, 256-byte aligned,
+ * for the call's exclusive use until `stream` reaches the end of the call
+ * (ATTN_ERR_WORKSPACE otherwise); it holds two chunks' inputs and outputs. The call is
+ * asynchronous on `stream`: the copies wait for the work queued on `stream` before the
+ * call, and work queued after it (or a synchronisation of `stream`) sees o and lse
+ * written. The compute runs on `stream`, the copies on two streams of the library's own.
+ * The other rules are attn_fwd's.
+ */
+ATTN_API attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o,
+                       float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                       float scale, int causal, const int32_t* kv_lens, attn_dtype_t dtype,
+                       void* workspace, size_t workspace_bytes, attn_stream_t stream);
+ATTN_API size_t attn_fwd_host_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                       attn_dtype_t dtype);
+
 /* Bytes of device workspace attn_bwd needs for these sizes (0 for an empty problem):
  * delta [B, Hq, Sq] fp32, plus, for bf16 GQA problems with fewer than 256 (batch, kv
  * head, 128-key tile) work items, fp32 partial dK and dV [B, Skv, Hkv * P, D] that a

@@ -274,3 +274,45 @@ def test_splitkv_needs_its_workspace(lib):
     assert call(D=80) == attn.ATTN_ERR_UNSUPPORTED
     assert call(q=A + 4) == attn.ATTN_ERR_INVALID_ARG
     assert call(B=0) == attn.ATTN_OK
+
+
+def test_fwd_host_workspace_size(lib):
+    f = attn.attn_fwd_host_workspace_size
+
+    def r256(n):
+        return (n + 255) // 256 * 256
+
+    # the DiT self-attention: 40 kv heads in 5 chunks of 8; two slots, each one chunk's
+    # Q, K, V, O (bf16), LSE and valid lengths
+    B, H, S, D = 1, 40, 32760, 128
+    slot = 4 * r256(B * S * 8 * D * 2) + r256(B * 8 * S * 4) + r256(B * 8 * 4)
+    assert f(B, H, H, S, S, D, attn.ATTN_BF16) == 2 * slot
+    # GQA 8 query heads on 2 kv heads: chunks of one kv head with its 4 query heads, fp32
+    B, Sq, Skv = 2, 100, 300
+    slot = (2 * r256(B * Sq * 4 * 64 * 4) + 2 * r256(B * Skv * 1 * 64 * 4) +
+            r256(B * 4 * Sq * 4) + r256(B * 1 * 4))
+    assert f(B, 8, 2, Sq, Skv, 64, attn.ATTN_F32) == 2 * slot
+    # empty problems and unsupported sizes need none
+    assert f(0, 40, 40, 10, 10, 128, attn.ATTN_BF16) == 0
+    assert f(1, 40, 40, 0, 10, 128, attn.ATTN_BF16) == 0
+    assert f(1, 40, 40, 10, 10, 80, attn.ATTN_BF16) == 0
+    assert f(1, 6, 4, 10, 10, 128, attn.ATTN_BF16) == 0
+
+
+def test_fwd_host_argument_checks(lib):
+    def call(**kw):
+        args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, Hq=40, Hkv=40, Sq=64, Skv=64, D=128,
+                    scale=0.088, causal=0, lens=None, dtype=attn.ATTN_BF16, ws=A,
+                    ws_bytes=1 << 40, stream=None)
+        args.update(kw)
+        return lib.attn_fwd_host(*args.values())
+    assert call(Hq=6, Hkv=4) == attn.ATTN_ERR_INVALID_ARG
+    assert call(D=80) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(scale=float("nan")) == attn.ATTN_ERR_INVALID_ARG
+    assert call(causal=2) == attn.ATTN_ERR_INVALID_ARG
+    assert call(q=None) == attn.ATTN_ERR_INVALID_ARG
+    assert call(ws=None) == attn.ATTN_ERR_WORKSPACE
+    assert call(ws_bytes=4096) == attn.ATTN_ERR_WORKSPACE
+    assert call(ws=A + 64) == attn.ATTN_ERR_WORKSPACE
+    assert call(B=0) == attn.ATTN_OK
+    assert call(Sq=0) == attn.ATTN_OK
