@@ -5,7 +5,9 @@ same launch configuration (the same entry points on the same workloads):
   the split-KV forward, against the whole oracle;
 * 64 query rows over the same cache through the split-KV forward, against the whole oracle;
 * the DiT self-attention through a 256-key paged cache with a shuffled block table: equal
-  bit for bit to the dense forward on the same keys, and the oracle on sampled rows.
+  bit for bit to the dense forward on the same keys, and the oracle on sampled rows;
+* the DiT self-attention from pinned host tensors (attn_fwd_host, the e2e call): equal bit
+  for bit to the dense forward.
 
 The scores are small (Q and K scaled by 0.5, so the softmax over 32760 keys is nearly
 uniform and |O| is about 0.005); the rel-L2 and max|diff|/max|ref| gates keep the checks
@@ -68,3 +70,26 @@ def test_paged_dit_self_attention_full_size():
                                              0, 0, rows)
         compare(f"c4_paged256:o[h={h}]", op[0, rows, h], o_ref, *TOL["bf16"]["o"], gate=GATE["bf16"])
         compare(f"c4_paged256:lse[h={h}]", lsep[0, h, rows], lse_ref, *TOL["bf16"]["lse"])
+
+
+def test_host_forward_dit_self_attention_full_size():
+    """The call bench.py times for the e2e figure of the DiT self-attention: attn_fwd_host
+    on pinned host tensors (five chunks of eight heads, copies overlapped with the compute)
+    gives attn_fwd's O and LSE bit for bit."""
+    w = workloads.get("c4")
+    inp = workloads.make_inputs(w)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Sq), device="cuda")
+    attn.attn_fwd(q, k, v, o, lse, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    o, lse = o.cpu(), lse.cpu()
+    del q, k, v
+    hq, hk, hv = (inp[n].pin_memory() for n in ("q", "k", "v"))
+    ho = torch.full(inp["q"].shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+    hlse = torch.full((w.B, w.Hq, w.Sq), float("nan")).pin_memory()
+    attn.attn_fwd_host(hq, hk, hv, ho, hlse, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert attn.attn_peek_device_error() == (attn.ATTN_OK, 0)
+    assert torch.equal(ho.view(torch.int16), o.view(torch.int16)), "host-path O differs"
+    assert torch.equal(hlse.view(torch.int32), lse.view(torch.int32)), "host-path LSE differs"
