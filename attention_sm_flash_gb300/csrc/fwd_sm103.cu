@@ -828,20 +828,20 @@ constexpr size_t fwd_smem_bytes() {
 constexpr int kMaxDev = 64;
 std::mutex g_mu;
 int g_num_sms[kMaxDev] = {};
-bool g_attr_set[kMaxDev][2][3] = {};
 
 template <int D, int NQ, int NK, int NV, int KIND>
 cudaError_t launch(const FwdParams& prm, int dev, cudaStream_t s) {
   constexpr size_t smem = fwd_smem_bytes<D, NQ, NK, NV>();
   static_assert(smem <= 232448, "shared memory per block");
   {
+    // the shared-memory opt-in, once per kernel instantiation and device
+    static bool attr_set[kMaxDev] = {};
     std::lock_guard<std::mutex> lk(g_mu);
-    const int which = D == 64 ? 0 : 1;
-    if (!g_attr_set[dev][which][KIND]) {
+    if (!attr_set[dev]) {
       cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D, NQ, NK, NV, KIND>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
-      g_attr_set[dev][which][KIND] = true;
+      attr_set[dev] = true;
     }
   }
   const int grid = prm.n_items < g_num_sms[dev] ? prm.n_items : g_num_sms[dev];
@@ -1011,6 +1011,10 @@ cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
   }
   if (kind == kPaged) return launch<128, 2, 2, 2, kPaged>(prm, dev, s);
   if (kind == kSplit) return launch<128, 2, 2, 2, kSplit>(prm, dev, s);
+  // short K/V (a few tiles per item, e.g. cross-attention to text tokens): one Q slot and
+  // three K slots, so that a K load of the next item does not wait for this item's first S
+  // (DiT cross-attention 498 -> 514 TFLOP/s; on long K/V the Q prefetch is worth more)
+  if (p.Skv <= 8 * kBN) return launch<128, 1, 3, 2, kDense>(prm, dev, s);
   return launch<128, 2, 2, 2, kDense>(prm, dev, s);
 }
 
