@@ -112,6 +112,7 @@ struct FwdCtl {
   int n_sorted;
   int sorted[kMaxSortedHeads];
   int lens[kMaxSortedHeads];
+  uint64_t pv_last;  // short K/V: an item's last PV product has been issued
 };
 
 struct Item {
@@ -254,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
       mbar_init(&c.p_full[b], kSoftThreads);
     }
     mbar_init(&c.o_free, kSoftThreads);
+    if (NQ == 1) mbar_init(&c.pv_last, 1);  // used by the short-K/V configuration only
     for (int q = 0; q < 4; ++q) {
       mbar_init(&c.xfull[q], 64);
       mbar_init(&c.xdone[q], 64);
@@ -476,7 +478,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
         if (s_role && !wait_phase(&c.q_full[qslot], (qpos / NQ) & 1, wc)) { ok = false; break; }
         ++qpos;
         tc_fence_after();
+        // Short K/V (one Q slot): the tensor pipe runs both issuers' products in one
+        // order, and an item's last PV is on the way to its epilogue, so the next item's
+        // first S waits until that PV has been issued (it then runs under the epilogue
+        // rather than ahead of the PV).
+        constexpr bool kPvFirst = NQ == 1;
         if (s_role) {
+          if (kPvFirst && ic > 0 && !wait_phase(&c.pv_last, (ic - 1) & 1, wc)) { ok = false; break; }
           // S(t) as soon as its K tile is in and the softmax has read S(t - 2)
           for (int t = 0; ok && t < it.n; ++t) ok = issue_s(qslot, t);
           if (!ok) break;
@@ -485,6 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
           // PV(t) once the softmax has written P(t)
           for (int t = 0; ok && t < it.n; ++t) ok = issue_pv(t, it.j0 + t, it.L);
           if (!ok) break;
+          if (kPvFirst) mbar_arrive(&c.pv_last);
         }
         kbase += it.n;
         ++ic;
