@@ -1020,10 +1020,11 @@ cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
   }
   if (kind == kPaged) return launch<128, 2, 2, 2, kPaged>(prm, dev, s);
   if (kind == kSplit) return launch<128, 2, 2, 2, kSplit>(prm, dev, s);
-  // short K/V (a few tiles per item, e.g. cross-attention to text tokens): one Q slot and
-  // three K slots, so that a K load of the next item does not wait for this item's first S
-  // (DiT cross-attention 498 -> 514 TFLOP/s; on long K/V the Q prefetch is worth more)
-  if (p.Skv <= 8 * kBN) return launch<128, 1, 3, 2, kDense>(prm, dev, s);
+  // short K/V (items of at most 16 tiles: cross-attention to text tokens, 2k-token
+  // training): one Q slot and three K slots, so that a K load of the next item does not
+  // wait for this item's first S (DiT cross-attention 498 -> 514 TFLOP/s, GQA profiling
+  // shape 880 -> 892; on long K/V the Q prefetch is worth more)
+  if (p.Skv <= 16 * kBN) return launch<128, 1, 3, 2, kDense>(prm, dev, s);
   return launch<128, 2, 2, 2, kDense>(prm, dev, s);
 }
 
