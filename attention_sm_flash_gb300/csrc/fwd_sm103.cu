@@ -301,14 +301,18 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
   const uint32_t tmem = c.tmem_base;
   WaitCtl wc{&c.abort, p.err, p.timeout_ns};
   // Registers: the control warpgroup (warps 0-3) gives 16 of its 168 to each thread of
-  // the two softmax warpgroups (measured: DiT self 1266 -> 1271, cross 536 -> 544 TFLOP/s;
-  // 136 / 184 spilled less gain than it cost). The split adds up to exactly the registers
-  // the block is launched with (384 x 168), which launch() checks before the first launch.
+  // the two softmax warpgroups (measured: cross-attention 533 -> 544 TFLOP/s, DiT self
+  // within noise; 136 / 184 was slower). The paged kernel keeps the plain allocation (the
+  // split cost it 5 %: its producer's page lookups need the registers). The split adds up
+  // to exactly the registers the block is launched with (384 x 168), which launch()
+  // checks before the first launch.
   static_assert(4 * 32 * kRegsCtl + 8 * 32 * kRegsSoft == kThreads * kRegsLaunch, "register split");
-  if (warp < 4)
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
-  else
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoft));
+  if constexpr (KIND != kPaged) {
+    if (warp < 4)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+    else
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoft));
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------- TMA producer
@@ -864,7 +868,7 @@ cudaError_t launch(const FwdParams& prm, int dev, cudaStream_t s) {
       cudaFuncAttributes fa{};
       cudaError_t ea = cudaFuncGetAttributes(&fa, fwd_sm103_kernel<D, NQ, NK, NV, KIND>);
       if (ea != cudaSuccess) return ea;
-      if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
+      if (KIND != kPaged && fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
       cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D, NQ, NK, NV, KIND>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
