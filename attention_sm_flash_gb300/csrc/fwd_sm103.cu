@@ -8,7 +8,7 @@
 // "same-GPU FA2/FA3 hardware comparison").
 //
 // One persistent CTA per SM (384 threads) loops over work items of 128 query rows (one Q
-// tile) of one (batch, head), taken in a longest-first order:
+// tile) of one (batch, head), listed longest first and dealt to the CTAs in a snake order:
 //   warp 0      TMA producer: a ring of Q tiles (the next item's Q is prefetched), and a
 //               ring of K/V tiles of 128 keys;
 //   warp 1      issues S = Q K^T into TMEM (one thread);
@@ -124,6 +124,15 @@ struct Item {
   int n;      // K/V tiles the item visits: j0 .. j0 + n - 1
   int split;  // key range of a split-KV item (0 otherwise)
 };
+
+// The item of this CTA's pass `pass`: the persistent CTAs take the items in a snake order
+// (CTA c takes c, 2G - 1 - c, 2G + c, ...), so that over a longest-first list (causal
+// query blocks) the CTA that took a pass's longest item takes the next pass's shortest.
+// Each pass still covers one contiguous block of items, as a plain round robin does.
+__device__ __forceinline__ int item_at(int pass) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return (pass & 1) ? (pass + 1) * G - 1 - c : pass * G + c;
+}
 
 __device__ __forceinline__ int clamp_len(int L, int Skv) { return L < 0 ? 0 : (L > Skv ? Skv : L); }
 
@@ -374,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
     uint32_t k_iss = 0, k_last = 0, v_iss = 0, v_last = 0;  // per slot: a load was issued / its parity
     uint32_t q_issued = 0, q_last = 0;                      // per Q slot
     bool ok = true, first = true;
-    for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+    for (int ps = 0, idx = item_at(0); ok && idx < p.n_items; idx = item_at(++ps)) {
       const Item it = decode_item<KIND>(idx, p, c);
       if (it.n == 0) continue;
       pc_k.base = -1;  // a new sequence: its block-table row
@@ -487,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
         ++gp;
         return true;
       };
-      for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+      for (int ps = 0, idx = item_at(0); ok && idx < p.n_items; idx = item_at(++ps)) {
         const Item it = decode_item<KIND>(idx, p, c);
         if (it.n == 0) continue;
         const uint32_t qslot = qpos % NQ;
@@ -526,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
     // in ring order (fix_req), so the fill this waits for is never ambiguous
     uint32_t kbase = 0, fr_par = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+    for (int ps = 0, idx = item_at(0); ok && idx < p.n_items; idx = item_at(++ps)) {
       const Item it = decode_item<KIND>(idx, p, c);
       if (it.n == 0) continue;
       for (int j = 0; j < it.n; ++j) {
@@ -582,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_sm103_kernel(const __grid_con
       ++xc;
       return true;
     };
-    for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+    for (int ps = 0, idx = item_at(0); ok && idx < p.n_items; idx = item_at(++ps)) {
       const Item it = decode_item<KIND>(idx, p, c);
       const int i = it.q0 + r;
       const bool row_ok = i < p.Sq;
