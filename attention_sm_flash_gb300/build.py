@@ -56,11 +56,41 @@ def _stamp(extra_flags) -> str:
     return h.hexdigest()
 
 
+def _code_text(src: bytes) -> bytes:
+    """The code of a C/C++/CUDA source without its comments, with every run of whitespace
+    made one space: what source_digest covers, so that editing a comment or the layout of
+    a file leaves the digest (and the figures recorded under it) as they were. String and
+    character literals are kept whole, comment markers inside them included."""
+    out = bytearray()
+    i, n = 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in b"\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == 0x5C else 1  # a backslash escapes the next byte
+            out += src[i:j + 1]
+            i = j + 1
+        elif src.startswith(b"//", i):
+            j = src.find(b"\n", i)
+            i = n if j < 0 else j
+            out += b" "
+        elif src.startswith(b"/*", i):
+            j = src.find(b"*/", i + 2)
+            i = n if j < 0 else j + 2
+            out += b" "
+        else:
+            out.append(c)
+            i += 1
+    return b" ".join(bytes(out).split())
+
+
 def source_digest(kernel_files=None) -> str:
-    """Hash of the CUDA sources and headers by relative path and content only (the same on
-    any machine and checkout path): the key under which measured per-kernel figures, such
-    as DRAM traffic, are recorded. ``kernel_files``: names of the .cu files that hold the
-    measured kernels (with every header, the code they include); None = all sources."""
+    """Hash of the code (comments and layout aside) of the CUDA sources and headers, by
+    relative path (the same on any machine and checkout path): the key under which
+    measured per-kernel figures, such as DRAM traffic, are recorded. ``kernel_files``:
+    names of the .cu files that hold the measured kernels (with every header, the code
+    they include); None = all sources."""
     h = hashlib.sha256()
     sources = _sources()
     if kernel_files is not None:
@@ -71,7 +101,7 @@ def source_digest(kernel_files=None) -> str:
     for f in sorted(files, key=lambda p: os.path.relpath(p, ROOT)):
         h.update(os.path.relpath(f, ROOT).encode())
         with open(f, "rb") as fh:
-            h.update(fh.read())
+            h.update(_code_text(fh.read()))
     return h.hexdigest()[:16]
 
 

@@ -8,7 +8,8 @@
 // "same-GPU FA2/FA3 hardware comparison").
 //
 // One persistent CTA per SM (384 threads) loops over work items of 128 query rows (one Q
-// tile) of one (batch, head), listed longest first and dealt to the CTAs in a snake order:
+// tile) of one (batch, head), listed longest first and dealt to the CTAs in a snake order
+// (round robin in the paged kind):
 //   warp 0      TMA producer: a ring of Q tiles (the next item's Q is prefetched), and a
 //               ring of K/V tiles of 128 keys;
 //   warp 1      issues S = Q K^T into TMEM (one thread);

@@ -316,3 +316,15 @@ def test_fwd_host_argument_checks(lib):
     assert call(ws=A + 64) == attn.ATTN_ERR_WORKSPACE
     assert call(B=0) == attn.ATTN_OK
     assert call(Sq=0) == attn.ATTN_OK
+
+
+def test_source_digest_covers_code_not_comments():
+    """The key of the recorded DRAM-traffic figures changes with the code only: comments and
+    layout are dropped, string and character literals are kept whole."""
+    from attention_sm_flash_gb300.build import _code_text
+    a = b'int a = 1; // a "note"\n/* block\n   comment */ const char* s = "x // y /* z */";\n'
+    b = b'int  a = 1;\n\n const char* s = "x // y /* z */"; // other note\n'
+    assert _code_text(a) == _code_text(b) == b'int a = 1; const char* s = "x // y /* z */";'
+    assert _code_text(b"char q = '\"'; int b; // c") == b"char q = '\"'; int b;"
+    assert _code_text(b"int a = 1;") != _code_text(b"int a = 2;")
+    assert _code_text(b'puts("a\\" // b");') == b'puts("a\\" // b");'
