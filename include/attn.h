@@ -169,9 +169,12 @@ ATTN_API attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void
 
 /* Bytes of device workspace attn_fwd_splitkv needs for these sizes: 0 when it does not
  * split (fp32, or enough (batch, head, query block) items: at least 152), else
- * n * B * Hq * Sq * (D + 1) * 4 bytes (each rounded up to 256) for n key ranges per item,
- * n = ceil(304 / items) capped so that each range holds at least 4 tiles of 128 keys.
- * A pure function of the sizes. */
+ * n * B * Hq * Sq * D * 4 bytes of partial O plus n * B * Hq * Sq * 4 bytes of partial LSE
+ * (each rounded up to 256) for n key ranges per item. With T tiles of 128 keys and I
+ * items, n is the count in 1 .. T / 4 (a range holds at least 4 tiles) that minimises a
+ * model of the time, ceil(I * n / 152) rounds of 2 * ceil(T / n) + 6 half-tile steps,
+ * then reduced to the number of ranges of ceil(T / n) tiles that cover T. A pure function
+ * of the sizes. */
 ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int D,
                                                 attn_dtype_t dtype);
 
