@@ -192,7 +192,11 @@ ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Hkv, int Sq, 
  * asynchronous on `stream`: the copies wait for the work queued on `stream` before the
  * call, and work queued after it (or a synchronisation of `stream`) sees o and lse
  * written. The compute runs on `stream`, the copies on two streams of the library's own.
- * The other rules are attn_fwd's.
+ * Argument errors are found before anything is queued. A CUDA error met while queueing the
+ * chunks is returned as ATTN_ERR_CUDA after some chunks' copies may already be queued:
+ * synchronize the device before reusing the workspace or the host buffers. Calls from
+ * several threads are serialised while they queue their work. The other rules are
+ * attn_fwd's.
  */
 ATTN_API attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o,
                        float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int D,
