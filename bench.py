@@ -254,6 +254,38 @@ def whole_job_tflops(flops_per_rank_step: float, ms_max: float, world: int) -> f
 
 
 # --------------------------------------------------------------------------- ours
+def bwd_kernel_estimates(key, dtype, bwd_ms, fwd_flops, peak):
+    """Per-kernel estimates for one backward call: each kernel's share of the recorded ncu
+    durations (profiles/bwd_kernel_durations.txt) times the call's CUDA-event time, and the
+    TFLOP/s of the GEMMs it executes over that time; None without a record for the current
+    code of the backward's kernels."""
+    path = os.path.join(HERE, "profiles", "bwd_kernel_durations.txt")
+    if not os.path.exists(path) or not bwd_ms:
+        return None
+    from attention_sm_flash_gb300 import build as libbuild
+    stamp = libbuild.source_digest(libbuild.OP_SOURCES.get(("attn_bwd", dtype)))
+    rows = []
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if line.startswith("#") or len(parts) != 5 or parts[0] != f"attn_bwd:{key}":
+                continue
+            if parts[4] != stamp:
+                return None
+            rows.append((parts[1], int(parts[2]), float(parts[3])))
+    total = sum(r[2] for r in rows)
+    if not rows or total <= 0:
+        return None
+    out = []
+    for name, gemms, us in rows:
+        ms = bwd_ms * us / total
+        tf = gemms * fwd_flops / 2 / (ms * 1e-3) / 1e12 if gemms else None
+        out.append({"kernel": name, "gemms": gemms, "ncu_share": round(us / total, 4),
+                    "ms_est": round(ms, 5), "tflops_est": round(tf, 1) if tf else None,
+                    "frac_est": round(tf / peak, 4) if tf else None})
+    return out
+
+
 def traffic_for(kernel_key, dtype="bf16"):
     """DRAM bytes per call recorded from an ncu capture of the current sources of that
     operation's kernels, or None (no record, or the kernels changed since)."""
@@ -406,7 +438,8 @@ def also_entry(bench, args, world, sampler_index, peaks, peak_src, dev):
         bwd_t = whole_job_tflops(bwd_fl, bm, world)
         out.update({"bwd_ms": round(bm, 5), "bwd_tflops": round(bwd_t, 3),
                     "bwd_frac": round(bwd_t / world / peak, 4),
-                    "bwd_traffic": traffic_for(f"attn_bwd:{w.key}", w.dtype)})
+                    "bwd_traffic": traffic_for(f"attn_bwd:{w.key}", w.dtype),
+                    "bwd_per_kernel_est": bwd_kernel_estimates(w.key, w.dtype, bm, fwd_fl, peak)})
     if w.key != "c3":
         op = {"dense": "attn_fwd", "split": "attn_fwd_splitkv"}.get(bench.mode, "attn_fwd_paged")
         out["fwd_traffic"] = traffic_for(f"{op}:{w.key}", w.dtype)
@@ -530,6 +563,8 @@ def run_ours(args, rank, world, local_rank):
                 "traffic": traffic_for(f"{dom}:{w.key}", w.dtype), "kernel": kernels[dom],
                 "call": dom, "peak_source": peak_note,
                 "algorithmic_flops_per_launch": dom_fl}
+    if dom == "attn_bwd":
+        roofline["per_kernel_est"] = bwd_kernel_estimates(w.key, w.dtype, bwd_mean, fwd_fl, peak)
     bf16_peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,

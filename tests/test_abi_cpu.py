@@ -328,3 +328,24 @@ def test_source_digest_covers_code_not_comments():
     assert _code_text(b"char q = '\"'; int b; // c") == b"char q = '\"'; int b;"
     assert _code_text(b"int a = 1;") != _code_text(b"int a = 2;")
     assert _code_text(b'puts("a\\" // b");') == b'puts("a\\" // b");'
+
+
+def test_backward_per_kernel_estimates_follow_the_recorded_shares(monkeypatch):
+    """bench.py's per-kernel backward figures: the recorded ncu shares scaled to the call's
+    time, GEMM FLOPs over each kernel's share; none once the backward's code changes."""
+    import bench
+    from attention_sm_flash_gb300 import build as libbuild
+    fwd_fl = 3.4376e10
+    est = bench.bwd_kernel_estimates("c3", "bf16", 0.14, fwd_fl, 1944.9)
+    assert est is not None and [e["kernel"].split("<")[0] for e in est] == [
+        "bwd_delta_kernel", "bwd_dq_sm103_kernel", "bwd_dkdv_sm103_kernel", "bwd_group_reduce_kernel"]
+    assert abs(sum(e["ncu_share"] for e in est) - 1.0) < 1e-3
+    assert abs(sum(e["ms_est"] for e in est) - 0.14) < 1e-4
+    dkdv = est[2]
+    assert dkdv["gemms"] == 4
+    want = 4 * fwd_fl / 2 / (dkdv["ms_est"] * 1e-3) / 1e12
+    assert abs(dkdv["tflops_est"] - want) < 0.1 and abs(dkdv["frac_est"] - want / 1944.9) < 1e-4
+    assert est[0]["tflops_est"] is None  # no GEMM in the delta kernel
+    assert bench.bwd_kernel_estimates("c1", "f32", 0.1, 1e6, 1.0) is None  # no record
+    monkeypatch.setattr(libbuild, "source_digest", lambda *a, **k: "0000000000000000")
+    assert bench.bwd_kernel_estimates("c3", "bf16", 0.14, fwd_fl, 1944.9) is None
